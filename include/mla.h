@@ -1,0 +1,182 @@
+/*
+ * mla.h -- C ABI of the B300 (sm_103a) Multi-head Latent Attention decode library.
+ *
+ * Sources, cited by page and section heading:
+ *   [0h-n0]  "論文解説: DeepSeek-V2 — MoEモデルのKVキャッシュを93.3%削減する
+ *            Multi-head Latent Attention" (0h-n0.github.io)
+ *   [kasblo] MLA explainer, kasblo.com
+ *   [qiita]  MLA notes, qiita.com/joule
+ *
+ * The problem statement these calls follow: during generation only the new
+ * token's query is computed while past keys/values come from a cache
+ * ([qiita] "MHA における KV Cache の問題"); MLA caches, per token and layer,
+ * the joint latent c^KV (d_c) and the shared RoPE key k^R (d_h^R) instead of
+ * per-head K and V ([0h-n0] "Decoupled RoPE"), and attends to that cache
+ * directly by absorbing W^UK into the query and W^UV into the output
+ * ([0h-n0] "行列吸収トリック"; [kasblo] "V側は、小さな表現の加重和を先に求める").
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer argument is a DEVICE pointer owned by the caller, 16-byte
+ *   aligned, row-major and densely packed with the shape given at the call.
+ *   The library never allocates or frees memory in these calls; the only
+ *   allocation is in mla_create (RoPE table, status word).
+ * - Floating-point buffers hold dims.dtype (bf16 or f32) unless stated
+ *   otherwise; lse is always f32.  Integer buffers are int32.
+ * - Calls are asynchronous on `stream`.  Arguments are validated on the host
+ *   before anything is launched; a rejected call launches nothing and
+ *   returns MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED or MLA_ERR_WORKSPACE.
+ *   A failed launch returns MLA_ERR_CUDA.
+ * - Values only the device can see (a block id outside the pool, a position
+ *   outside the RoPE table, a sequence shorter than its query count) are
+ *   checked in the kernels: the offending access is skipped and a bit is set
+ *   in the handle's device status word, read back by
+ *   mla_check_device_status.  Every wait inside a kernel is bounded; a wait
+ *   that runs out sets MLA_ERR_DEVICE_TIMEOUT there as well.
+ * - A call with zero tokens is a valid no-op.
+ * - Head i owns rows [i*d_h, (i+1)*d_h) of W^UQ, W^UK, W^UV and rows
+ *   [i*d_hr, (i+1)*d_hr) of W^QR; W^O consumes the head-major concatenation.
+ * - RoPE rotates interleaved pairs (x[2k], x[2k+1]) by pos * rope_base^(-2k/d_hr),
+ *   positions 0-based; the cos/sin table is computed on the host in double.
+ */
+#ifndef MLA_H
+#define MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size, inconsistent dims */
+  MLA_ERR_UNSUPPORTED = 2,    /* valid request this build does not implement */
+  MLA_ERR_WORKSPACE = 3,      /* workspace pointer null or smaller than required */
+  MLA_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
+  MLA_ERR_DEVICE_TIMEOUT = 5, /* a bounded device-side wait ran out */
+  MLA_ERR_DEVICE_BOUNDS = 6   /* a device-side index check failed; access skipped */
+} mla_status;
+
+typedef enum { MLA_BF16 = 0, MLA_F32 = 1 } mla_dtype;
+
+/* Layer sizes in the pages' notation ([0h-n0] "技術的詳細"; [qiita]
+ * "Multi-Head Latent Attention"): n_h heads of width d_h, RoPE width d_hr
+ * (d_h^R), KV latent d_c, query latent d_cq (d_c'), hidden d_model (d).
+ * block = cache rows per block of the paged pool.  scale multiplies every
+ * score; 1/sqrt(d_h + d_hr) per [qiita] "Attention 計算". */
+typedef struct {
+  int n_h, d_h, d_hr, d_c, d_cq, d_model, block;
+  float rope_base;
+  float scale;
+  mla_dtype dtype;
+} mla_dims;
+
+typedef struct mla_handle mla_handle;
+
+/* Creates a handle on the current CUDA device: copies dims, builds the RoPE
+ * cos/sin table for positions [0, max_pos) and a 4-byte device status word.
+ * Rejects odd d_hr, non-positive sizes, max_pos < 1.  *out is owned by the
+ * caller and released with mla_destroy. */
+mla_status mla_create(const mla_dims* dims, int max_pos, mla_handle** out);
+void mla_destroy(mla_handle* h);
+const char* mla_status_string(mla_status s);
+
+/* Number of streaming multiprocessors the handle plans for, and whether the
+ * tcgen05 path serves these dims (n_h=128, d_c=512, d_hr=64, block=64, bf16). */
+int mla_num_sms(const mla_handle* h);
+int mla_uses_tensor_path(const mla_handle* h);
+
+/* Upper bound, in device polls, on every bounded wait of later launches
+ * (0 = library default). Used to exercise the timeout path. */
+mla_status mla_set_wait_limit(mla_handle* h, long long polls);
+
+/* ---- a0: query projection --------------------------------------------------
+ * [qiita] "Query の圧縮": c^Q = W^DQ x, q^C_i = W^UQ_i c^Q;
+ * [qiita] "RoPE の扱い": q^R_i = W^QR_i c^Q (returned before the rotation,
+ * which mla_absorb_q applies).
+ *   x    [n_tok, d_model]     w_dq [d_cq, d_model]
+ *   w_uq [n_h*d_h, d_cq]      w_qr [n_h*d_hr, d_cq]
+ *   q_c  [n_tok, n_h, d_h]    q_r  [n_tok, n_h, d_hr]   (outputs)
+ *   ws: mla_q_proj_workspace_bytes(h, n_tok) bytes (holds c^Q). */
+size_t mla_q_proj_workspace_bytes(const mla_handle* h, int n_tok);
+mla_status mla_q_proj(mla_handle* h, const void* x, const void* w_dq, const void* w_uq,
+                      const void* w_qr, int n_tok, void* q_c, void* q_r, void* ws,
+                      size_t ws_bytes, cudaStream_t stream);
+
+/* ---- a1: cache append ------------------------------------------------------
+ * [0h-n0] "MLA: 低ランクKV結合圧縮": c^KV_t = W^DKV h_t; [qiita] "RoPE の扱い":
+ * k^R_t = RoPE(W^KR h_t); [0h-n0] "Decoupled RoPE": the cached row is
+ * [c^KV_t ; k^R_t], d_c + d_hr elements, k^R stored after the rotation.
+ *   x          [n_new, d_model]     new tokens' hidden states
+ *   w_dkr      [d_c + d_hr, d_model] rows 0..d_c-1 = W^DKV, rows d_c.. = W^KR
+ *   seq_idx    [n_new]  sequence of each new token, in [0, batch)
+ *   pos        [n_new]  its 0-based position in that sequence
+ *   block_table[batch, max_blocks]  physical block of each logical block
+ *   pool       [n_pool_blocks, block, d_c + d_hr]  (written)
+ * Row of token (b, p) = block_table[b*max_blocks + p/block]*block + p%block.
+ * A block id outside [0, n_pool_blocks) or p/block >= max_blocks skips the
+ * row and sets MLA_ERR_DEVICE_BOUNDS. */
+mla_status mla_cache_append(mla_handle* h, const void* x, const void* w_dkr, const int* seq_idx,
+                            const int* pos, int n_new, const int* block_table, int max_blocks,
+                            int batch, void* pool, int n_pool_blocks, cudaStream_t stream);
+
+/* ---- a2: query absorption --------------------------------------------------
+ * [0h-n0] "行列吸収トリック": q~_i = W^UK_i^T q^C_i (d_c), and q^R_i rotated at
+ * the token's position ([qiita] "RoPE の扱い").
+ *   q_c [n_tok, n_h, d_h]   q_r [n_tok, n_h, d_hr] (raw)   pos [n_tok]
+ *   w_uk [n_h*d_h, d_c]
+ *   q_lat [n_tok, n_h, d_c + d_hr] = [q~_i ; RoPE_pos(q^R_i)]   (output) */
+mla_status mla_absorb_q(mla_handle* h, const void* q_c, const void* q_r, const int* pos,
+                        int n_tok, const void* w_uk, void* q_lat, cudaStream_t stream);
+
+/* ---- a3 + a4: latent attention over the paged cache -----------------------
+ * [qiita] "Attention 計算" in absorbed form: s_ij = scale*(q~_i.c_j + q^R_i.k^R_j)
+ * for every cached row j <= t (t = the query's position), softmax over j,
+ * o~_i = sum_j a_ij c_j ([kasblo] "V側は、小さな表現の加重和を先に求める"),
+ * lse_i = ln sum_j exp(s_ij).
+ *   q_lat [n_tok, n_h, d_c + d_hr]
+ *   pool, n_pool_blocks, block_table, max_blocks: as in mla_cache_append
+ *   seq_lens [batch]  cached rows of each sequence INCLUDING this step's tokens
+ *   cu_q [batch+1]    query tokens of sequence b are rows cu_q[b]..cu_q[b+1]-1;
+ *                     they sit at positions seq_lens[b]-q_len .. seq_lens[b]-1
+ *                     and see rows 0..their own position (causal, inclusive)
+ *   num_workers       0 = one worker per available SM pair; otherwise the
+ *                     number of workers the keys are spread over.  Keys of a
+ *                     token split across workers are merged by a log-sum-exp
+ *                     combine (not on the pages).
+ *   ws                mla_decode_workspace_bytes(h, n_tok, num_workers) bytes
+ *   o_lat [n_tok, n_h, d_c]  (output, dims.dtype)   lse [n_tok, n_h] f32 (output)
+ * n_tok must equal cu_q[batch] (checked on the device). */
+size_t mla_decode_workspace_bytes(const mla_handle* h, int n_tok, int num_workers);
+mla_status mla_decode(mla_handle* h, const void* q_lat, const void* pool, int n_pool_blocks,
+                      const int* block_table, int max_blocks, const int* seq_lens,
+                      const int* cu_q, int batch, int n_tok, int num_workers, void* ws,
+                      size_t ws_bytes, void* o_lat, float* lse, cudaStream_t stream);
+
+/* ---- a5: output ------------------------------------------------------------
+ * o_i = W^UV_i o~_i ([kasblo] "V側は、小さな表現の加重和を先に求める") and
+ * u = W^O [o_1; ...; o_n_h] ([qiita] "Attention 計算").
+ *   o_lat [n_tok, n_h, d_c]   w_uv [n_h*d_h, d_c]   w_o [d_model, n_h*d_h]
+ *   u [n_tok, d_model] (output)
+ *   ws: mla_out_workspace_bytes(h, n_tok) bytes (holds the per-head o_i). */
+size_t mla_out_workspace_bytes(const mla_handle* h, int n_tok);
+mla_status mla_out(mla_handle* h, const void* o_lat, const void* w_uv, const void* w_o,
+                   int n_tok, void* u, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Synchronises `stream`, returns the first error any kernel recorded in the
+ * device status word since the last check (MLA_OK if none) and clears it. */
+mla_status mla_check_device_status(mla_handle* h, cudaStream_t stream);
+
+/* Runs one kernel that waits on a barrier no one arrives at, with the
+ * handle's wait limit; it must come back with MLA_ERR_DEVICE_TIMEOUT recorded
+ * in the status word.  Exercises the bounded-wait path without a fault. */
+mla_status mla_selftest_wait_timeout(mla_handle* h, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H */
