@@ -1,0 +1,430 @@
+"""Benchmark of one MLA decode step on B300 (see the design doc for the recipe).
+
+Workload (default): DeepSeek-V2 attention layer (d=5120, n_h=128, d_h=128,
+d_h^R=64, d_c=512, d_c'=1536), batched decode B=64 sequences of T=4096 cached
+rows each, one new token per sequence, 64-row cache blocks scattered over a
+seeded random permutation of the pool.  One step = the whole path for the 64
+new tokens: query projection, cache append, W^UK absorption, latent attention
+(+ split combine), W^UV / W^O output.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  Under torchrun every rank runs an independent replica
+on its own GPU (the path has no exchange step); the time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from head_latent_attention_26_b300 import synth  # noqa: E402
+
+METRIC = "MLA decode tokens/s and latent-cache GB/s (% of HBM/tensor roofline), 1×B300"
+B_DEFAULT, T_DEFAULT = 64, 4096
+SEED = 1003
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p["bf16_tflops_sustained"], "measured"
+    except (OSError, KeyError, ValueError):
+        return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    return ws, rank
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        sm.sort()
+        med = sm[len(sm) // 2] if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+
+def make_workload(B: int, T: int, device="cuda"):
+    """Weights, a pool holding T-1 prior rows per sequence, and the step's inputs."""
+    d = synth.V2
+    W = synth.weights(d, SEED, device=device)
+    W_dkr = torch.cat([W["W_dkv"], W["W_kr"]], dim=0).contiguous()
+    lens = [T] * B
+    table, n_blocks = synth.block_table(lens, d.block, SEED)
+    table = table.to(device)
+    pool = torch.empty(n_blocks, d.block, d.width, dtype=torch.bfloat16, device=device)
+    flat = pool.view(-1, d.width)
+    # prior rows: c ~ N(0,1), k^R ~ N(0,1), the distribution W^DKV h and RoPE(W^KR h)
+    # have for h ~ N(0,1), W ~ N(0, 1/fan_in)
+    for b0 in range(0, B, 8):
+        nb = min(8, B - b0)
+        rows = synth.normal((nb * T, d.width), SEED + b0, "prior_rows", device=device)
+        j = torch.arange(T, device=device)
+        for k in range(nb):
+            slots = table[b0 + k][j // d.block].long() * d.block + (j % d.block)
+            flat[slots] = rows[k * T:(k + 1) * T]
+        del rows
+    x = synth.hidden(B, d, SEED, name="h_new", device=device)
+    inp = {
+        "x": x,
+        "seq_idx": torch.arange(B, dtype=torch.int32, device=device),
+        "pos": torch.full((B,), T - 1, dtype=torch.int32, device=device),
+        "seq_lens": torch.full((B,), T, dtype=torch.int32, device=device),
+        "cu_q": torch.arange(B + 1, dtype=torch.int32, device=device),
+    }
+    return d, W, W_dkr, table, pool, inp
+
+
+def algorithmic(B: int, T: int, d=synth.V2):
+    """Bytes and flops the decode kernel must move / do (one launch)."""
+    cache = B * T * d.width * 2
+    q = B * d.n_h * d.width * 2
+    out = B * d.n_h * d.d_c * 2 + B * d.n_h * 4
+    flops = B * d.n_h * T * (2 * d.width + 2 * d.d_c)
+    return cache, cache + q + out, flops
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    ws, rank = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    from head_latent_attention_26_b300 import build
+    build.build()
+    from head_latent_attention_26_b300 import mla
+    B, T = args.batch, args.seq_len
+    d, W, W_dkr, table, pool, inp = make_workload(B, T)
+    m = mla.MLA(d, T + 64, torch.bfloat16)
+    assert m.tensor_path
+    bufs = {
+        "q_c": torch.empty(B, d.n_h, d.d_h, dtype=torch.bfloat16, device="cuda"),
+        "q_r": torch.empty(B, d.n_h, d.d_hr, dtype=torch.bfloat16, device="cuda"),
+        "q_lat": torch.empty(B, d.n_h, d.width, dtype=torch.bfloat16, device="cuda"),
+        "o_lat": torch.empty(B, d.n_h, d.d_c, dtype=torch.bfloat16, device="cuda"),
+        "lse": torch.empty(B, d.n_h, dtype=torch.float32, device="cuda"),
+        "u": torch.empty(B, d.d_model, dtype=torch.bfloat16, device="cuda"),
+    }
+    ws_dec = m.workspace("decode", m.decode_workspace_bytes(B, args.num_workers))
+    dec_ev = []
+
+    def step(x, time_decode=False):
+        m.q_proj(x, W["W_dq"], W["W_uq"], W["W_qr"], bufs["q_c"], bufs["q_r"])
+        m.cache_append(x, W_dkr, inp["seq_idx"], inp["pos"], table, pool)
+        m.absorb_q(bufs["q_c"], bufs["q_r"], inp["pos"], W["W_uk"], bufs["q_lat"])
+        if time_decode:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+        m.decode(bufs["q_lat"], pool, table, inp["seq_lens"], inp["cu_q"], args.num_workers, bufs["o_lat"],
+                 bufs["lse"], ws_dec)
+        if time_decode:
+            e1.record()
+            dec_ev.append((e0, e1))
+        m.out(bufs["o_lat"], W["W_uv"], W["W_o"], bufs["u"])
+
+    for _ in range(args.warmup):
+        step(inp["x"])
+    m.check()
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        step(inp["x"], time_decode=True)
+    t1.record()
+    barrier()
+    clk = clocks.stop()
+    m.check()
+    ms = t0.elapsed_time(t1) / args.steps
+    dec_ms = sum(a.elapsed_time(b) for a, b in dec_ev) / len(dec_ev)
+    launches_per_step = 3 + 1 + 1 + 3 + 2  # q_proj, append, absorb, plan+decode+combine, out
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs, the step, D2H of u -- all inside the timed region
+    h_x = inp["x"].cpu().pin_memory()
+    h_pos = inp["pos"].cpu().pin_memory()
+    h_lens = inp["seq_lens"].cpu().pin_memory()
+    h_u = torch.empty(B, d.d_model, dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(inp["x"])
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        x_dev.copy_(h_x, non_blocking=True)
+        inp["pos"].copy_(h_pos, non_blocking=True)
+        inp["seq_lens"].copy_(h_lens, non_blocking=True)
+        step(x_dev)
+        h_u.copy_(bufs["u"], non_blocking=True)
+    e1.record()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    m.check()
+
+    times = torch.tensor([ms, dec_ms, e2e_ms], dtype=torch.float64, device="cuda")
+    if ws > 1:
+        import torch.distributed as dist
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    ms, dec_ms, e2e_ms = times.tolist()
+    if rank != 0:
+        return None
+
+    hbm, tf_burst, tf_sus, src = _peaks()
+    cache_b, dec_bytes, flops = algorithmic(B, T, d)
+    t = dec_ms * 1e-3
+    gbs = dec_bytes / t / 1e9
+    tflops = flops / t / 1e12
+    # binding roofline of the decode kernel: the slower of HBM and tensor at the
+    # measured peaks (sustained tensor peak: the kernel runs inside a long loop)
+    t_hbm, t_tc = dec_bytes / (hbm * 1e9), flops / (tf_sus * 1e12)
+    if t_tc >= t_hbm:
+        roof = {"bound": "tensor", "achieved": round(tflops, 1), "peak": tf_sus, "unit": "TFLOP/s",
+                "frac": round(tflops / tf_sus, 4)}
+    else:
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4)}
+    roof.update(kernel="decode_tc_kernel (+plan, combine)", peak_source=f"{src} (MEASURED_PEAKS.json)",
+                traffic=args.traffic, other={"hbm": {"achieved_gbs": round(gbs, 1), "peak": hbm,
+                                                     "frac": round(gbs / hbm, 4)},
+                                             "tensor": {"achieved_tflops": round(tflops, 1),
+                                                        "peak_sustained": tf_sus, "peak_burst": tf_burst,
+                                                        "frac_sustained": round(tflops / tf_sus, 4),
+                                                        "frac_burst": round(tflops / tf_burst, 4)}},
+                algorithmic_bytes=dec_bytes, algorithmic_flops=flops, decode_us=round(dec_ms * 1e3, 2))
+    n = ws
+    value = B * n / (ms * 1e-3)
+    res = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": n,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"MLA decode step, DeepSeek-V2 layer, B={B} sequences x T={T} cached rows, "
+                               "64-row blocks in a permuted pool, 1 new token per sequence",
+                   "batch": B, "seq_len": T, "num_workers": args.num_workers,
+                   "parallelism": f"replicas x{n}" if n > 1 else "single GPU",
+                   "l2": "no flush: the step reads > L2 (302 MB cache + 300 MB weights)"},
+        "latent_cache_gbs": round(cache_b / t / 1e9, 1),
+        "decode_tokens_per_s": round(B * n / t, 1),
+        "roofline": roof,
+        "e2e": {"value": round(B * n / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h_x.numel() * 2 + h_pos.numel() * 4 + h_lens.numel() * 4,
+                "d2h_bytes_per_step": h_u.numel() * 2},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(B, T, budget_s=args.cpu_budget)
+    return res
+
+
+# ---------------------------------------------------------------------------
+# oracle on the host cores (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_inputs(B: int):
+    """Weights and new-token states for the oracle legs, drawn on the host
+    (same recipe and seeds; the host generator's values differ from the
+    device generator's, which does not matter for timing)."""
+    import oracle as O
+    d = synth.V2
+    W = synth.weights(d, SEED, device="cpu")
+    return {k: O.f64(v) for k, v in W.items()}, synth.hidden(B, d, SEED, name="h_new", device="cpu")
+
+
+def _prior_rows(B: int, T: int, b: int):
+    d = synth.V2
+    b0 = (b // 8) * 8
+    g = synth.normal((min(8, B - b0) * T, d.width), SEED + b0, "prior_rows", device="cpu")
+    return g[(b - b0) * T:(b - b0 + 1) * T]
+
+
+def _oracle_token(Wn, x, rows_bf16, T: int, b: int):
+    """The oracle, as it stands, for token b of the workload: its cache row,
+    query, expanded K/V over the sequence's T rows, softmax, W^O.  Returns u."""
+    import numpy as np
+    import oracle as O
+    d = synth.V2
+    rows = O.f64(rows_bf16)
+    c_new, kr_new = O.kv_latent(O.f64(x[b:b + 1]), Wn["W_dkv"], Wn["W_kr"], [T - 1], d.rope_base)
+    c = np.concatenate([rows[:T - 1, :d.d_c], c_new])
+    k_r = np.concatenate([rows[:T - 1, d.d_c:], kr_new])
+    _, q_c, q_r_raw = O.query_parts(O.f64(x[b:b + 1]), Wn["W_dq"], Wn["W_uq"], Wn["W_qr"], d.n_h)
+    o, _ = O.attend_expanded(q_c[0], O.rope(q_r_raw[0], T - 1, d.rope_base), c, k_r, Wn["W_uk"], Wn["W_uv"])
+    return O.output_projection(o, Wn["W_o"])
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:  # noqa: BLE001
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(B: int, T: int, budget_s: float = 15.0):
+    """Time the fp64 oracle on whole tokens of the workload until budget_s of
+    oracle arithmetic has run (input generation is outside the timer)."""
+    t_start = time.perf_counter()
+    Wn, x = _oracle_inputs(B)
+    done, elapsed = 0, 0.0
+    while done < B and (done == 0 or elapsed < budget_s):
+        rows = _prior_rows(B, T, done)
+        t0 = time.perf_counter()
+        _oracle_token(Wn, x, rows, T, done)
+        elapsed += time.perf_counter() - t0
+        done += 1
+    return {"value": round(done / elapsed, 4), "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"{done} of {B} tokens of the B={B}, T={T} workload (expanded K/V, fp64 numpy), "
+                      f"{elapsed:.1f} s of oracle time; input generation untimed",
+            "wall_s": round(time.perf_counter() - t_start, 1)}
+
+
+def run_reference(args):
+    ws, rank = _dist()
+    if rank != 0:
+        return None
+    B, T = args.batch, args.seq_len
+    Wn, x = _oracle_inputs(B)
+    total_s = 0.0
+    for s in range(args.warmup + args.steps):
+        rows = _prior_rows(B, T, s % B)
+        t0 = time.perf_counter()
+        _oracle_token(Wn, x, rows, T, s % B)
+        if s >= args.warmup:
+            total_s += time.perf_counter() - t0
+    v = args.steps / total_s
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(v, 4),
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_s / args.steps * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"MLA decode step, DeepSeek-V2 layer, B={B} sequences x T={T} cached rows, "
+                               "64-row blocks in a permuted pool, 1 new token per sequence",
+                   "batch": B, "seq_len": T},
+        "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+                         "sample": f"each step = 1 of the B={B} tokens through the fp64 oracle "
+                                   "(expanded K/V); input generation untimed"},
+        "e2e": {"value": round(v, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--batch", type=int, default=B_DEFAULT)
+    ap.add_argument("--seq-len", type=int, default=T_DEFAULT)
+    ap.add_argument("--num-workers", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per decode launch from an ncu capture of this kernel version")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        res = run_reference(args)
+    else:
+        res = run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,745 @@
+// decode_tc.cu -- latent-cache attention on sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// What it computes ([qiita] "Attention 計算", absorbed form of [0h-n0]
+// "行列吸収トリック" and [kasblo] "V側は、小さな表現の加重和を先に求める"):
+//   s_ij  = scale * (q~_i . c_j + q^R_i . k^R_j)   for every cached row j <= t
+//   o~_i  = sum_j softmax_j(s_ij) c_j,   lse_i = ln sum_j exp(s_ij)
+// for all 128 heads i of one query token at once: the heads form the M = 128
+// dimension of every MMA, each 64-row cache block is one key tile.
+//
+// Layout of the work (fixed sizes: n_h = 128, d_c = 512, d_hr = 64, block = 64):
+// * A worker is a cluster of two CTAs.  CTA c owns latent columns
+//   [256c, 256c+256) and RoPE columns [512+32c, 512+32c+32) of every cached
+//   row; it TMA-loads only those 288 columns of each key tile (36 KB).
+// * Scores: CTA c computes the partial score over its 288 columns,
+//   S_c = Q~[:, own] . C[:, own]^T  (M=128, N=64, K=288), with the latent part
+//   of Q~ resident in TMEM (A operand) and its RoPE part in shared memory.
+// * The two partial score tiles are swapped through distributed shared memory;
+//   both CTAs add them (fp32, commutative, so bit-identical) and run the same
+//   online softmax, so no softmax state needs to be exchanged.
+// * Values: CTA c accumulates O[:, own 256 latent columns] += P . C[:, own]
+//   (M=128, N=256, K=64) in TMEM, reading the same shared-memory key tile as
+//   an MN-major B operand.  No K or V is ever expanded.
+// * Rescaling of O is lazy: the running max only moves when a tile's max
+//   exceeds it by more than 2^8, which keeps every exp2 argument <= 8 and the
+//   result exact (numerator and denominator share the stale max).
+// * Keys of a token can be split across workers (balanced contiguous ranges of
+//   the global tile list); split pieces write fp32 partials that a separate
+//   log-sum-exp combine kernel merges.
+//
+// Warp roles per CTA (192 threads): warp 0 = TMA producer, warp 1 = MMA
+// issuer + TMEM owner, warps 2..5 = "row" warps, thread = head (TMEM lane).
+// Every wait is bounded; a wait that runs out records MLA_ERR_DEVICE_TIMEOUT,
+// raises a CTA-wide abort flag and the roles drain and exit.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kHeads = 128;
+constexpr int kTile = 64;               // keys per tile = rows per cache block
+constexpr int kWidth = 576;             // d_c + d_hr
+constexpr int kDc = 512;
+constexpr int kStages = 4;
+constexpr uint32_t kBoxBytes = 64 * 128;                    // 64 keys x 64 cols bf16
+constexpr uint32_t kRopeBoxBytes = 64 * 64;                 // 64 keys x 32 cols bf16
+constexpr uint32_t kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;  // 36864
+constexpr uint32_t kQRopeBytes = kHeads * 64;               // 128 heads x 32 cols bf16
+constexpr uint32_t kInboxBytes = kHeads * 256;              // 128 heads x 64 fp32
+constexpr uint32_t kOffStages = 0;
+constexpr uint32_t kOffQRope = kOffStages + kStages * kStageBytes;
+constexpr uint32_t kOffInbox = kOffQRope + kQRopeBytes;
+constexpr uint32_t kOffBars = kOffInbox + 2 * kInboxBytes;
+constexpr uint32_t kSmemBytes = kOffBars + 256 + 1024;      // + alignment slack
+// TMEM columns (512 allocated): O half | S partial | Q~ latent half | P
+constexpr uint32_t kTmemO = 0, kTmemS = 256, kTmemQ = 320, kTmemP = 448;
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct Maps {
+  CUtensorMap latent;  // pool as [rows, 576] bf16, box 64 cols x 64 rows, 128B swizzle
+  CUtensorMap rope;    // same tensor, box 32 cols x 64 rows, 64B swizzle
+};
+
+struct Params {
+  const __nv_bfloat16* q_lat;
+  const int* block_table;
+  const int* seq_lens;
+  const int* cu_q;
+  const int* prefix;  // [n_tok+1] tiles before each token (workspace)
+  __nv_bfloat16* o_lat;
+  float* lse;
+  float* part_o;      // [2W][128][512]
+  float* part_lse;    // [2W][128]
+  int* status;
+  long long wait_limit;
+  int max_blocks, batch, n_tok, n_pool_blocks, workers;
+  float scale_log2;
+};
+
+struct Bars {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t q_ready, s_full, s_free, p_ready, o_done;
+  uint64_t xin_full[2], xout_free[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Params& p, Bars* bs,
+                                         bool cluster_scope = false) {
+  for (long long i = 0;; ++i) {
+    if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (i >= p.wait_limit || *reinterpret_cast<volatile int*>(&bs->abort)) {
+      report(p.status, MLA_ERR_DEVICE_TIMEOUT);
+      atomicExch(&bs->abort, 1);
+      return false;
+    }
+  }
+}
+
+// Contiguous slice [lo, hi) of the global tile list handled by worker g.
+__device__ __forceinline__ void worker_range(int g, int workers, int total, int& lo, int& hi) {
+  lo = static_cast<int>(static_cast<long long>(g) * total / workers);
+  hi = static_cast<int>(static_cast<long long>(g + 1) * total / workers);
+}
+
+__device__ __forceinline__ int first_token_at(const int* prefix, int n_tok, int x) {
+  // largest n with prefix[n] <= x (tiles of token n are [prefix[n], prefix[n+1]))
+  int lo = 0, hi = n_tok - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(prefix + mid) <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct Unit {
+  int n;          // query token
+  int ta, tb;     // tile range within the token
+  int pos;        // token position (last visible key)
+  int b;          // sequence
+  int slot;       // partial slot, or -1 when the unit covers the whole token
+};
+
+// Iterates the units of a worker; every role walks the same list.
+struct UnitIter {
+  int x, hi, n, first;
+  __device__ bool next(const Params& p, int g, Unit& u) {
+    while (x < hi) {
+      const int t0 = __ldg(p.prefix + n), t1 = __ldg(p.prefix + n + 1);
+      if (t1 <= x) { ++n; continue; }
+      u.n = n;
+      u.ta = x - t0;
+      u.tb = min(hi, t1) - t0;
+      u.b = seq_of_token(p.cu_q, p.batch, n);
+      u.pos = __ldg(p.seq_lens + u.b) - (__ldg(p.cu_q + u.b + 1) - n);
+      const bool complete = (u.ta == 0 && u.tb == t1 - t0);
+      u.slot = complete ? -1 : 2 * g + (first ? 0 : 1);
+      first = 0;
+      x = t0 + u.tb;
+      ++n;
+      return true;
+    }
+    return false;
+  }
+};
+
+__device__ __forceinline__ UnitIter make_iter(const Params& p, int g) {
+  const int total = __ldg(p.prefix + p.n_tok);
+  UnitIter it;
+  worker_range(g, p.workers, total, it.x, it.hi);
+  it.n = it.x < it.hi ? first_token_at(p.prefix, p.n_tok, it.x) : 0;
+  it.first = 1;
+  return it;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bs = reinterpret_cast<Bars*>(smem + kOffBars);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t c = cluster_ctarank();  // which half of the columns this CTA owns
+  const uint32_t peer = c ^ 1u;
+  const int g = blockIdx.x >> 1;         // worker index
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bs->full[s], 1);
+      mbar_init(&bs->empty[s], 1);
+    }
+    mbar_init(&bs->q_ready, 4);
+    mbar_init(&bs->s_full, 1);
+    mbar_init(&bs->s_free, 4);
+    mbar_init(&bs->p_ready, 4);
+    mbar_init(&bs->o_done, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bs->xin_full[s], 128);
+      mbar_init(&bs->xout_free[s], 128);
+    }
+    mbar_init(&bs->drain, 1);
+    bs->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bs->tmem_base, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  cluster_arrive();  // peer barriers are initialised before any remote arrive
+  cluster_wait();
+  tc_fence_after();
+  const uint32_t tmem = bs->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&maps.latent);
+      tma_prefetch_desc(&maps.rope);
+      UnitIter iter = make_iter(p, g);
+      Unit u;
+      uint32_t it = 0;
+      bool ok = true;
+      while (ok && iter.next(p, g, u)) {
+        for (int t = u.ta; t < u.tb && ok; ++t, ++it) {
+          const int s = it % kStages;
+          if (it >= kStages) ok = wait_bar(&bs->empty[s], ((it / kStages) - 1) & 1, p, bs);
+          if (!ok) break;
+          int blk = t < p.max_blocks ? __ldg(p.block_table + static_cast<size_t>(u.b) * p.max_blocks + t) : -1;
+          if (blk < 0 || blk >= p.n_pool_blocks) {
+            report(p.status, MLA_ERR_DEVICE_BOUNDS);
+            blk = 0;
+          }
+          uint8_t* st = smem + kOffStages + s * kStageBytes;
+          mbar_arrive_expect_tx(&bs->full[s], kStageBytes);
+          const int y = blk * kTile;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tma_load_2d(st + j * kBoxBytes, &maps.latent, &bs->full[s], 256 * c + 64 * j, y);
+          tma_load_2d(st + 4 * kBoxBytes, &maps.rope, &bs->full[s], 512 + 32 * c, y);
+        }
+      }
+      // drain: every issued stage must land before the CTA may exit
+      if (!ok) {
+        for (uint32_t k = (it > kStages ? it - kStages : 0); k < it; ++k)
+          for (long long i = 0; i < p.wait_limit && !mbar_try_wait(&bs->full[k % kStages], (k / kStages) & 1); ++i) {
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
+      const uint32_t idesc_o = idesc_bf16_f32(128, 256, false, true);
+      const uint32_t qrope = smem_u32(smem + kOffQRope);
+      UnitIter iter = make_iter(p, g);
+      Unit u;
+      uint32_t it = 0, n_units = 0, sfree_n = 0, pready_n = 0;
+      bool ok = true;
+      auto issue_s = [&](uint32_t k) {
+        const uint32_t st = smem_u32(smem + kOffStages + (k % kStages) * kStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+          const uint64_t bd = smem_desc(st + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+          mma_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, idesc_s, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const uint64_t ad = smem_desc(qrope + kk * 32, 16, 512, kSwizzle64B);
+          const uint64_t bd = smem_desc(st + 4 * kBoxBytes + kk * 32, 16, 512, kSwizzle64B);
+          mma_ss(tmem + kTmemS, ad, bd, idesc_s, 1);
+        }
+        mma_commit(&bs->s_full);
+      };
+      while (ok && iter.next(p, g, u)) {
+        ok = wait_bar(&bs->q_ready, n_units & 1, p, bs);
+        ++n_units;
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t it0 = it;
+        ok = wait_bar(&bs->full[it % kStages], (it / kStages) & 1, p, bs);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(it);
+        for (int t = u.ta; t < u.tb && ok; ++t, ++it) {
+          if (t + 1 < u.tb) {
+            ok = wait_bar(&bs->full[(it + 1) % kStages], ((it + 1) / kStages) & 1, p, bs) &&
+                 wait_bar(&bs->s_free, sfree_n & 1, p, bs);
+            ++sfree_n;
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(it + 1);
+          } else {
+            ++sfree_n;  // the last tile's drain completes before the next q_ready
+          }
+          ok = wait_bar(&bs->p_ready, pready_n & 1, p, bs);
+          ++pready_n;
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + kOffStages + (it % kStages) * kStageBytes);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t bd = smem_desc(st + ks * 2048, 8192, 1024, kSwizzle128B);
+            mma_ts(tmem + kTmemO, tmem + kTmemP + ks * 8, bd, idesc_o, (it > it0 || ks > 0) ? 1u : 0u);
+          }
+          mma_commit(&bs->o_done);
+          mma_commit(&bs->empty[it % kStages]);
+        }
+      }
+      if (!ok) {
+        // every issued MMA must finish before TMEM is released
+        mma_commit(&bs->drain);
+        for (long long i = 0; i < p.wait_limit && !mbar_try_wait(&bs->drain, 0); ++i) {
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ row warps
+    const int q = warp & 3;                // TMEM lane quadrant of this warp
+    const int r = q * 32 + lane;           // head = TMEM lane
+    const int tr = threadIdx.x - 64;       // 0..127 among the row warps
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    uint8_t* inbox = smem + kOffInbox;
+    const uint32_t inbox_local = smem_u32(inbox);
+    const uint32_t inbox_peer = map_to_rank(inbox_local, peer);
+    const uint32_t xin_full_peer[2] = {map_to_rank(smem_u32(&bs->xin_full[0]), peer),
+                                       map_to_rank(smem_u32(&bs->xin_full[1]), peer)};
+    const uint32_t xout_free_peer[2] = {map_to_rank(smem_u32(&bs->xout_free[0]), peer),
+                                        map_to_rank(smem_u32(&bs->xout_free[1]), peer)};
+    UnitIter iter = make_iter(p, g);
+    Unit u;
+    uint32_t it = 0, sfull_n = 0, odone_n = 0;
+    bool ok = true;
+    while (ok && iter.next(p, g, u)) {
+      // ---- latent query: own 256 latent columns -> TMEM, own 32 RoPE columns -> smem
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(p.q_lat + (static_cast<size_t>(u.n) * kHeads + r) * kWidth + 256 * c);
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t v[16];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 w = __ldg(src + ch * 4 + j);
+            v[4 * j] = w.x; v[4 * j + 1] = w.y; v[4 * j + 2] = w.z; v[4 * j + 3] = w.w;
+          }
+          tmem_st16(tmem + lane_base + kTmemQ + ch * 16, v);
+          // second half of this 64-column chunk
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 w = __ldg(src + ch * 4 + 16 + j);
+            v[4 * j] = w.x; v[4 * j + 1] = w.y; v[4 * j + 2] = w.z; v[4 * j + 3] = w.w;
+          }
+          tmem_st16(tmem + lane_base + kTmemQ + 64 + ch * 16, v);
+        }
+        const uint4* rsrc = reinterpret_cast<const uint4*>(p.q_lat + (static_cast<size_t>(u.n) * kHeads + r) * kWidth + 512 + 32 * c);
+        uint8_t* qr = smem + kOffQRope + r * 64;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) *reinterpret_cast<uint4*>(qr + ((ch ^ ((r >> 1) & 3)) * 16)) = __ldg(rsrc + ch);
+        tmem_st_wait();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bs->q_ready);
+      }
+      float m = -INFINITY, l = 0.f;
+      for (int t = u.ta; t < u.tb && ok; ++t, ++it) {
+        const bool first = (t == u.ta);
+        // ---- 1. own partial scores out of TMEM
+        ok = wait_bar(&bs->s_full, sfull_n & 1, p, bs);
+        ++sfull_n;
+        if (!ok) break;
+        tc_fence_after();
+        float s[64];
+        {
+          uint32_t v[16];
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            tmem_ld16(tmem + lane_base + kTmemS + ch * 16, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) s[ch * 16 + j] = __uint_as_float(v[j]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bs->s_free);
+        // ---- 2. swap partial scores with the peer CTA
+        const uint32_t slot = it & 1;
+        if (it >= 2) {
+          ok = wait_bar(&bs->xout_free[slot], ((it >> 1) - 1) & 1, p, bs, true);
+          if (!ok) break;
+        }
+        {
+          const uint32_t dst = inbox_peer + slot * kInboxBytes + r * 256;
+#pragma unroll
+          for (int ch = 0; ch < 16; ++ch)
+            st_cluster_v4(dst + ((ch ^ (r & 15)) * 16), s[4 * ch], s[4 * ch + 1], s[4 * ch + 2], s[4 * ch + 3]);
+          mbar_arrive_cluster(xin_full_peer[slot]);
+        }
+        ok = wait_bar(&bs->xin_full[slot], (it >> 1) & 1, p, bs, true);
+        if (!ok) break;
+        {
+          const uint8_t* src = inbox + slot * kInboxBytes + r * 256;
+#pragma unroll
+          for (int ch = 0; ch < 16; ++ch) {
+            const float4 w = *reinterpret_cast<const float4*>(src + ((ch ^ (r & 15)) * 16));
+            s[4 * ch] += w.x; s[4 * ch + 1] += w.y; s[4 * ch + 2] += w.z; s[4 * ch + 3] += w.w;
+          }
+          mbar_arrive_cluster(xout_free_peer[slot]);
+        }
+        // ---- 3. online softmax in the log2 domain, causal mask on the last tile
+        const int valid = min(kTile, u.pos - t * kTile + 1);  // keys of this tile the token sees
+        float mt = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          s[j] = (j < valid) ? s[j] * p.scale_log2 : -INFINITY;
+          mt = fmaxf(mt, s[j]);
+        }
+        float m_use = m, f = 1.f;
+        if (first) {
+          m_use = mt;
+        } else if (mt > m + kRescaleThreshold) {
+          m_use = mt;
+          f = exp2f(m - mt);
+        }
+        uint32_t pk[32];
+        float rowsum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(exp2f(s[2 * j] - m_use), exp2f(s[2 * j + 1] - m_use));
+          const float2 back = __bfloat1622float2(b2);
+          rowsum += back.x + back.y;
+          pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+        l = first ? rowsum : l * f + rowsum;
+        m = m_use;
+        // ---- 4. wait for the previous O MMA, rescale O if the max moved, write P
+        if (!first) {
+          ok = wait_bar(&bs->o_done, odone_n & 1, p, bs);
+          ++odone_n;
+          if (!ok) break;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, f != 1.f)) {
+#pragma unroll 1
+            for (int ch = 0; ch < 16; ++ch) {
+              uint32_t v[16];
+              tmem_ld16(tmem + lane_base + kTmemO + ch * 16, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * f);
+              tmem_st16(tmem + lane_base + kTmemO + ch * 16, v);
+            }
+          }
+        }
+        tmem_st16(tmem + lane_base + kTmemP, pk);
+        tmem_st16(tmem + lane_base + kTmemP + 16, pk + 16);
+        tmem_st_wait();
+        // rows past the token's position may hold anything: zero them for the O MMA
+        if (valid < kTile) {
+          uint8_t* st = smem + kOffStages + (it % kStages) * kStageBytes;
+          for (int idx = tr; idx < (kTile - valid) * 32; idx += 128) {
+            const int row = valid + (idx >> 5), box = (idx >> 3) & 3, ch = idx & 7;
+            *reinterpret_cast<uint4*>(st + box * kBoxBytes + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          asm volatile("bar.sync 1, 128;" ::: "memory");  // all four row warps zeroed their share
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bs->p_ready);
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l for this head and this CTA's 256 latent columns
+      ok = wait_bar(&bs->o_done, odone_n & 1, p, bs);
+      ++odone_n;
+      if (!ok) break;
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const float lse_val = (m + log2f(l)) * 0.69314718055994531f;
+      if (u.slot < 0) {
+        __nv_bfloat16* dst = p.o_lat + (static_cast<size_t>(u.n) * kHeads + r) * kDc + 256 * c;
+#pragma unroll 1
+        for (int ch = 0; ch < 16; ++ch) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_base + kTmemO + ch * 16, v);
+          tmem_ld_wait();
+          uint32_t o[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            o[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * inv_l, __uint_as_float(v[2 * j + 1]) * inv_l);
+          reinterpret_cast<uint4*>(dst + ch * 16)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          reinterpret_cast<uint4*>(dst + ch * 16)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        if (c == 0) p.lse[static_cast<size_t>(u.n) * kHeads + r] = lse_val;
+      } else {
+        float* dst = p.part_o + (static_cast<size_t>(u.slot) * kHeads + r) * kDc + 256 * c;
+#pragma unroll 1
+        for (int ch = 0; ch < 16; ++ch) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_base + kTmemO + ch * 16, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            reinterpret_cast<float4*>(dst + ch * 16)[j] =
+                make_float4(__uint_as_float(v[4 * j]) * inv_l, __uint_as_float(v[4 * j + 1]) * inv_l,
+                            __uint_as_float(v[4 * j + 2]) * inv_l, __uint_as_float(v[4 * j + 3]) * inv_l);
+        }
+        if (c == 0) p.part_lse[static_cast<size_t>(u.slot) * kHeads + r] = lse_val;
+      }
+      tc_fence_before();
+    }
+  }
+
+  __syncthreads();
+  cluster_arrive();  // no CTA leaves while its peer may still touch its shared memory
+  cluster_wait();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// prefix[n] = tiles of all tokens before n; tiles of token n = pos_n/64 + 1.
+__global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ seq_lens, const int* __restrict__ cu_q,
+                                                    int batch, int n_tok, int max_blocks, int* __restrict__ prefix,
+                                                    int* status) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry;
+  if (threadIdx.x == 0) { carry = 0; prefix[0] = 0; }
+  if (threadIdx.x == 0 && __ldg(cu_q + batch) != n_tok) report(status, MLA_ERR_DEVICE_BOUNDS);
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int base = 0; base < n_tok; base += 1024) {
+    const int n = base + threadIdx.x;
+    int tiles = 0;
+    if (n < n_tok) {
+      const int b = seq_of_token(cu_q, batch, n);
+      const int pos = __ldg(seq_lens + b) - (__ldg(cu_q + b + 1) - n);
+      if (pos < 0 || n < __ldg(cu_q + b) || n >= __ldg(cu_q + b + 1) || pos / kTile >= max_blocks) {
+        report(status, MLA_ERR_DEVICE_BOUNDS);
+        tiles = pos >= 0 ? min(pos / kTile + 1, max_blocks) : 0;
+      } else {
+        tiles = pos / kTile + 1;
+      }
+    }
+    int v = tiles;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane == 31) warp_sums[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int incl = v + (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
+    if (n < n_tok) prefix[n + 1] = incl;
+    __syncthreads();
+    if (threadIdx.x == 1023) carry = incl;
+    __syncthreads();
+  }
+}
+
+__device__ __forceinline__ int worker_of(long long x, int workers, int total) {
+  int g = static_cast<int>(x * workers / total);
+  while (g + 1 < workers && static_cast<long long>(g + 1) * total / workers <= x) ++g;
+  while (g > 0 && static_cast<long long>(g) * total / workers > x) --g;
+  return g;
+}
+
+// Partial slot that worker g wrote for token n: slot 2g when n is the token
+// its range starts in, else 2g+1; -1 for a worker with an empty range.
+__device__ __forceinline__ int piece_slot(const int* prefix, int n_tok, int workers, int total, int g, int n) {
+  int lo, hi;
+  worker_range(g, workers, total, lo, hi);
+  if (lo >= hi) return -1;
+  return 2 * g + (first_token_at(prefix, n_tok, lo) == n ? 0 : 1);
+}
+
+// Merge the pieces of every token whose keys were split across workers:
+// lse = ln sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s.  One warp per head;
+// the log-sum-exp over pieces is a warp-shuffle reduction.
+__global__ void __launch_bounds__(256) combine_kernel(const int* __restrict__ prefix, int n_tok, int workers,
+                                                      const float* __restrict__ part_o,
+                                                      const float* __restrict__ part_lse,
+                                                      __nv_bfloat16* __restrict__ o_lat, float* __restrict__ lse) {
+  const int n = blockIdx.x;
+  const int total = __ldg(prefix + n_tok);
+  const int t0 = __ldg(prefix + n), t1 = __ldg(prefix + n + 1);
+  if (t1 <= t0) return;
+  const int g0 = worker_of(t0, workers, total), g1 = worker_of(t1 - 1, workers, total);
+  if (g0 == g1) return;  // whole token inside one worker: already final
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int npieces = g1 - g0 + 1;
+  for (int h = blockIdx.y * 8 + warp; h < kHeads; h += 8 * gridDim.y) {
+    // pass 1: L = ln sum exp(lse_s)
+    float mx = -INFINITY;
+    for (int k = lane; k < npieces; k += 32) {
+      const int slot = piece_slot(prefix, n_tok, workers, total, g0 + k, n);
+      if (slot >= 0) mx = fmaxf(mx, __ldg(part_lse + static_cast<size_t>(slot) * kHeads + h));
+    }
+    mx = warp_max(mx);
+    float sum = 0.f;
+    for (int k = lane; k < npieces; k += 32) {
+      const int slot = piece_slot(prefix, n_tok, workers, total, g0 + k, n);
+      if (slot >= 0) sum += expf(__ldg(part_lse + static_cast<size_t>(slot) * kHeads + h) - mx);
+    }
+    sum = warp_sum(sum);
+    const float L = mx + logf(sum);
+    // pass 2: weighted sum of the pieces, 16 columns per lane
+    float acc[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+    for (int k = 0; k < npieces; ++k) {
+      const int slot = piece_slot(prefix, n_tok, workers, total, g0 + k, n);
+      if (slot < 0) continue;
+      const float w = expf(__ldg(part_lse + static_cast<size_t>(slot) * kHeads + h) - L);
+      const float4* src = reinterpret_cast<const float4*>(part_o + (static_cast<size_t>(slot) * kHeads + h) * kDc);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 v = __ldg(src + lane + 32 * j);
+        acc[4 * j] += w * v.x; acc[4 * j + 1] += w * v.y; acc[4 * j + 2] += w * v.z; acc[4 * j + 3] += w * v.w;
+      }
+    }
+    __nv_bfloat16* dst = o_lat + (static_cast<size_t>(n) * kHeads + h) * kDc;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = 4 * (lane + 32 * j);
+      reinterpret_cast<uint2*>(dst + col)[0] = make_uint2(pack_bf16x2(acc[4 * j], acc[4 * j + 1]),
+                                                          pack_bf16x2(acc[4 * j + 2], acc[4 * j + 3]));
+    }
+    if (lane == 0) lse[static_cast<size_t>(n) * kHeads + h] = L;
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+bool encode_pool_map(CUtensorMap* m, const void* pool, long long rows, uint32_t box_cols, CUtensorMapSwizzle sw) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kWidth), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kWidth) * 2};
+  cuuint32_t box[2] = {box_cols, static_cast<cuuint32_t>(kTile)};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int resolve_workers(const mla_handle* h, int num_workers) {
+  return num_workers > 0 ? num_workers : max(1, h->num_sms / 2);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+size_t decode_tc_workspace_bytes(const mla_handle* h, int n_tok, int num_workers) {
+  const size_t W = static_cast<size_t>(resolve_workers(h, num_workers));
+  return align256(sizeof(int) * (static_cast<size_t>(n_tok) + 1)) + align256(sizeof(float) * 2 * W * kHeads * kDc) +
+         align256(sizeof(float) * 2 * W * kHeads);
+}
+
+cudaError_t launch_decode_tc(const mla_handle* h, const void* q_lat, const void* pool, int n_pool_blocks,
+                             const int* block_table, int max_blocks, const int* seq_lens, const int* cu_q,
+                             int batch, int n_tok, int num_workers, void* ws, size_t ws_bytes, void* o_lat,
+                             float* lse, cudaStream_t s) {
+  const int W = resolve_workers(h, num_workers);
+  Maps maps;
+  const long long rows = static_cast<long long>(n_pool_blocks) * kTile;
+  if (!encode_pool_map(&maps.latent, pool, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_pool_map(&maps.rope, pool, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  Params prm;
+  prm.prefix = reinterpret_cast<int*>(w);
+  w += align256(sizeof(int) * (static_cast<size_t>(n_tok) + 1));
+  prm.part_o = reinterpret_cast<float*>(w);
+  w += align256(sizeof(float) * 2 * static_cast<size_t>(W) * kHeads * kDc);
+  prm.part_lse = reinterpret_cast<float*>(w);
+  prm.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
+  prm.block_table = block_table;
+  prm.seq_lens = seq_lens;
+  prm.cu_q = cu_q;
+  prm.o_lat = static_cast<__nv_bfloat16*>(o_lat);
+  prm.lse = lse;
+  prm.status = h->status;
+  prm.wait_limit = h->wait_limit;
+  prm.max_blocks = max_blocks;
+  prm.batch = batch;
+  prm.n_tok = n_tok;
+  prm.n_pool_blocks = n_pool_blocks;
+  prm.workers = W;
+  prm.scale_log2 = h->dims.scale * kLog2e;
+
+  plan_kernel<<<1, 1024, 0, s>>>(seq_lens, cu_q, batch, n_tok, max_blocks, const_cast<int*>(prm.prefix), h->status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  decode_tc_kernel<<<2 * W, kThreads, kSmemBytes, s>>>(maps, prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  combine_kernel<<<dim3(n_tok, 2), 256, 0, s>>>(prm.prefix, n_tok, W, prm.part_o, prm.part_lse, prm.o_lat, lse);
+  return cudaGetLastError();
+}
+
+}  // namespace mla
+
+namespace mla {
+namespace {
+// Waits on a barrier that nothing ever arrives at, with the bounded wait of
+// the decode kernel; must return having recorded MLA_ERR_DEVICE_TIMEOUT.
+__global__ void wait_timeout_selftest_kernel(int* status, long long wait_limit) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool done = false;
+    for (long long i = 0; i < wait_limit && !done; ++i) done = mbar_try_wait(&bar, 0);
+    if (!done) report(status, MLA_ERR_DEVICE_TIMEOUT);
+    mbar_arrive(&bar);  // complete the phase so the barrier is idle at exit
+  }
+}
+}  // namespace
+
+cudaError_t launch_wait_timeout_selftest(const mla_handle* h, cudaStream_t s) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(h->status, h->wait_limit);
+  return cudaGetLastError();
+}
+}  // namespace mla

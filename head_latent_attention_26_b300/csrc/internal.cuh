@@ -1,0 +1,87 @@
+// internal.cuh -- handle layout, device status word, scalar helpers shared by
+// the kernels of the library (not part of the public ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mla.h"
+
+struct mla_handle {
+  mla_dims dims;
+  int max_pos;
+  int device;
+  int num_sms;
+  float* rope_cos;  // [max_pos, d_hr/2], cos(pos * base^(-2k/d_hr)) rounded from double
+  float* rope_sin;
+  int* status;      // first device-side error code, 0 = none
+  long long wait_limit;
+  bool tensor_path;
+};
+
+namespace mla {
+
+constexpr long long kDefaultWaitLimit = 1ll << 26;  // mbarrier polls before giving up
+
+// Records `code` in the status word unless an earlier error is already there.
+__device__ __forceinline__ void report(int* status, int code) { atomicCAS(status, 0, code); }
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T>
+__device__ __forceinline__ T from_f(float x);
+template <>
+__device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Sequence owning query row n: the largest b with cu_q[b] <= n.
+__device__ __forceinline__ int seq_of_token(const int* cu_q, int batch, int n) {
+  int lo = 0, hi = batch - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (cu_q[mid] <= n) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+}  // namespace mla
+
+// ---- launchers implemented in the kernel translation units ----------------
+namespace mla {
+cudaError_t launch_linear(const mla_handle* h, const void* X, int ldx, const void* W, int in, int out,
+                          void* Y, int ldy, int n_tok, cudaStream_t s);
+cudaError_t launch_cache_append_simt(const mla_handle* h, const void* x, const void* w_dkr,
+                                     const int* seq_idx, const int* pos, int n_new,
+                                     const int* block_table, int max_blocks, int batch, void* pool,
+                                     int n_pool_blocks, cudaStream_t s);
+cudaError_t launch_absorb_q_simt(const mla_handle* h, const void* q_c, const void* q_r, const int* pos,
+                                 int n_tok, const void* w_uk, void* q_lat, cudaStream_t s);
+cudaError_t launch_decode_simt(const mla_handle* h, const void* q_lat, const void* pool,
+                               int n_pool_blocks, const int* block_table, int max_blocks,
+                               const int* seq_lens, const int* cu_q, int batch, int n_tok, void* o_lat,
+                               float* lse, cudaStream_t s);
+cudaError_t launch_up_project_simt(const mla_handle* h, const void* o_lat, const void* w_uv, int n_tok,
+                                   void* o, cudaStream_t s);
+cudaError_t launch_wait_timeout_selftest(const mla_handle* h, cudaStream_t s);
+
+// tcgen05 decode (dims n_h=128, d_c=512, d_hr=64, block=64, bf16)
+size_t decode_tc_workspace_bytes(const mla_handle* h, int n_tok, int num_workers);
+cudaError_t launch_decode_tc(const mla_handle* h, const void* q_lat, const void* pool,
+                             int n_pool_blocks, const int* block_table, int max_blocks,
+                             const int* seq_lens, const int* cu_q, int batch, int n_tok,
+                             int num_workers, void* ws, size_t ws_bytes, void* o_lat, float* lse,
+                             cudaStream_t s);
+}  // namespace mla

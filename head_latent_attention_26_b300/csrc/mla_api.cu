@@ -1,0 +1,230 @@
+// mla_api.cu -- the C ABI declared in include/mla.h: handle life cycle,
+// host-side argument checks, dispatch to the kernels.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "internal.cuh"
+#include "mla.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+size_t elem_bytes(const mla_handle* h) { return h->dims.dtype == MLA_BF16 ? 2 : 4; }
+
+#define MLA_TRY_CUDA(expr)                            \
+  do {                                                \
+    cudaError_t e_ = (expr);                          \
+    if (e_ != cudaSuccess) return MLA_ERR_CUDA;       \
+  } while (0)
+
+bool dims_ok(const mla_dims* d) {
+  return d && d->n_h > 0 && d->d_h > 0 && d->d_hr >= 2 && d->d_hr % 2 == 0 && d->d_c > 0 &&
+         d->d_cq > 0 && d->d_model > 0 && d->block > 0 && d->rope_base > 0.f &&
+         std::isfinite(d->scale) && d->scale > 0.f && (d->dtype == MLA_BF16 || d->dtype == MLA_F32);
+}
+
+// Shapes the generic path handles: the latent sum keeps d_c/32 values per lane.
+bool simt_ok(const mla_dims* d) { return d->d_c <= 512; }
+
+bool tensor_path_dims(const mla_dims* d) {
+  return d->n_h == 128 && d->d_c == 512 && d->d_hr == 64 && d->block == 64 && d->dtype == MLA_BF16;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported";
+    case MLA_ERR_WORKSPACE: return "workspace missing or too small";
+    case MLA_ERR_CUDA: return "CUDA error";
+    case MLA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case MLA_ERR_DEVICE_BOUNDS: return "device-side index check failed";
+  }
+  return "unknown status";
+}
+
+mla_status mla_create(const mla_dims* dims, int max_pos, mla_handle** out) {
+  if (!out) return MLA_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!dims_ok(dims) || max_pos < 1) return MLA_ERR_INVALID_ARG;
+  if (!simt_ok(dims)) return MLA_ERR_UNSUPPORTED;
+  mla_handle* h = new mla_handle();
+  h->dims = *dims;
+  h->max_pos = max_pos;
+  h->wait_limit = mla::kDefaultWaitLimit;
+  h->tensor_path = tensor_path_dims(dims);
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+    delete h;
+    return MLA_ERR_CUDA;
+  }
+  // RoPE angles pos * base^(-2k/d_hr) in double, cos/sin rounded to float.
+  const int half = dims->d_hr / 2;
+  const size_t n = static_cast<size_t>(max_pos) * half;
+  std::vector<float> c(n), s(n);
+  for (int p = 0; p < max_pos; ++p)
+    for (int k = 0; k < half; ++k) {
+      const double theta = std::pow(static_cast<double>(dims->rope_base), -2.0 * k / dims->d_hr);
+      const double ang = static_cast<double>(p) * theta;
+      c[static_cast<size_t>(p) * half + k] = static_cast<float>(std::cos(ang));
+      s[static_cast<size_t>(p) * half + k] = static_cast<float>(std::sin(ang));
+    }
+  bool ok = cudaMalloc(&h->rope_cos, n * sizeof(float)) == cudaSuccess &&
+            cudaMalloc(&h->rope_sin, n * sizeof(float)) == cudaSuccess &&
+            cudaMalloc(&h->status, sizeof(int)) == cudaSuccess &&
+            cudaMemcpy(h->rope_cos, c.data(), n * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(h->rope_sin, s.data(), n * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemset(h->status, 0, sizeof(int)) == cudaSuccess;
+  if (!ok) {
+    mla_destroy(h);
+    return MLA_ERR_CUDA;
+  }
+  *out = h;
+  return MLA_OK;
+}
+
+void mla_destroy(mla_handle* h) {
+  if (!h) return;
+  if (h->rope_cos) cudaFree(h->rope_cos);
+  if (h->rope_sin) cudaFree(h->rope_sin);
+  if (h->status) cudaFree(h->status);
+  delete h;
+}
+
+int mla_num_sms(const mla_handle* h) { return h ? h->num_sms : 0; }
+int mla_uses_tensor_path(const mla_handle* h) { return h && h->tensor_path ? 1 : 0; }
+
+mla_status mla_set_wait_limit(mla_handle* h, long long polls) {
+  if (!h || polls < 0) return MLA_ERR_INVALID_ARG;
+  h->wait_limit = polls == 0 ? mla::kDefaultWaitLimit : polls;
+  return MLA_OK;
+}
+
+// ---------------------------------------------------------------- a0
+size_t mla_q_proj_workspace_bytes(const mla_handle* h, int n_tok) {
+  if (!h || n_tok < 0) return 0;
+  return (static_cast<size_t>(n_tok) * h->dims.d_cq * elem_bytes(h) + 255) & ~static_cast<size_t>(255);
+}
+
+mla_status mla_q_proj(mla_handle* h, const void* x, const void* w_dq, const void* w_uq, const void* w_qr,
+                      int n_tok, void* q_c, void* q_r, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!h || n_tok < 0) return MLA_ERR_INVALID_ARG;
+  if (n_tok == 0) return MLA_OK;
+  for (const void* p : {x, w_dq, w_uq, w_qr, static_cast<const void*>(q_c), static_cast<const void*>(q_r)})
+    if (!p || !aligned16(p)) return MLA_ERR_INVALID_ARG;
+  if (!ws || !aligned16(ws) || ws_bytes < mla_q_proj_workspace_bytes(h, n_tok)) return MLA_ERR_WORKSPACE;
+  const mla_dims& d = h->dims;
+  MLA_TRY_CUDA(mla::launch_linear(h, x, d.d_model, w_dq, d.d_model, d.d_cq, ws, d.d_cq, n_tok, stream));
+  MLA_TRY_CUDA(mla::launch_linear(h, ws, d.d_cq, w_uq, d.d_cq, d.n_h * d.d_h, q_c, d.n_h * d.d_h, n_tok,
+                                  stream));
+  MLA_TRY_CUDA(mla::launch_linear(h, ws, d.d_cq, w_qr, d.d_cq, d.n_h * d.d_hr, q_r, d.n_h * d.d_hr,
+                                  n_tok, stream));
+  return MLA_OK;
+}
+
+// ---------------------------------------------------------------- a1
+mla_status mla_cache_append(mla_handle* h, const void* x, const void* w_dkr, const int* seq_idx,
+                            const int* pos, int n_new, const int* block_table, int max_blocks, int batch,
+                            void* pool, int n_pool_blocks, cudaStream_t stream) {
+  if (!h || n_new < 0) return MLA_ERR_INVALID_ARG;
+  if (n_new == 0) return MLA_OK;
+  if (!x || !w_dkr || !pool || !aligned16(x) || !aligned16(w_dkr) || !aligned16(pool))
+    return MLA_ERR_INVALID_ARG;
+  if (!seq_idx || !pos || !block_table || !aligned4(seq_idx) || !aligned4(pos) || !aligned4(block_table))
+    return MLA_ERR_INVALID_ARG;
+  if (max_blocks < 1 || batch < 1 || n_pool_blocks < 1) return MLA_ERR_INVALID_ARG;
+  MLA_TRY_CUDA(mla::launch_cache_append_simt(h, x, w_dkr, seq_idx, pos, n_new, block_table, max_blocks,
+                                             batch, pool, n_pool_blocks, stream));
+  return MLA_OK;
+}
+
+// ---------------------------------------------------------------- a2
+mla_status mla_absorb_q(mla_handle* h, const void* q_c, const void* q_r, const int* pos, int n_tok,
+                        const void* w_uk, void* q_lat, cudaStream_t stream) {
+  if (!h || n_tok < 0) return MLA_ERR_INVALID_ARG;
+  if (n_tok == 0) return MLA_OK;
+  for (const void* p : {q_c, q_r, w_uk, static_cast<const void*>(q_lat)})
+    if (!p || !aligned16(p)) return MLA_ERR_INVALID_ARG;
+  if (!pos || !aligned4(pos)) return MLA_ERR_INVALID_ARG;
+  MLA_TRY_CUDA(mla::launch_absorb_q_simt(h, q_c, q_r, pos, n_tok, w_uk, q_lat, stream));
+  return MLA_OK;
+}
+
+// ---------------------------------------------------------------- a3 + a4
+size_t mla_decode_workspace_bytes(const mla_handle* h, int n_tok, int num_workers) {
+  if (!h || n_tok < 0 || num_workers < 0) return 0;
+  if (h->tensor_path) return mla::decode_tc_workspace_bytes(h, n_tok, num_workers);
+  return 0;
+}
+
+mla_status mla_decode(mla_handle* h, const void* q_lat, const void* pool, int n_pool_blocks,
+                      const int* block_table, int max_blocks, const int* seq_lens, const int* cu_q,
+                      int batch, int n_tok, int num_workers, void* ws, size_t ws_bytes, void* o_lat,
+                      float* lse, cudaStream_t stream) {
+  if (!h || n_tok < 0 || batch < 0 || num_workers < 0) return MLA_ERR_INVALID_ARG;
+  if (n_tok == 0) return MLA_OK;
+  if (batch < 1 || max_blocks < 1 || n_pool_blocks < 1) return MLA_ERR_INVALID_ARG;
+  for (const void* p : {q_lat, pool, static_cast<const void*>(o_lat), static_cast<const void*>(lse)})
+    if (!p || !aligned16(p)) return MLA_ERR_INVALID_ARG;
+  for (const int* p : {block_table, seq_lens, cu_q})
+    if (!p || !aligned4(p)) return MLA_ERR_INVALID_ARG;
+  const size_t need = mla_decode_workspace_bytes(h, n_tok, num_workers);
+  if (need > 0 && (!ws || !aligned16(ws) || ws_bytes < need)) return MLA_ERR_WORKSPACE;
+  if (h->tensor_path) {
+    MLA_TRY_CUDA(mla::launch_decode_tc(h, q_lat, pool, n_pool_blocks, block_table, max_blocks, seq_lens,
+                                       cu_q, batch, n_tok, num_workers, ws, ws_bytes, o_lat, lse, stream));
+  } else {
+    MLA_TRY_CUDA(mla::launch_decode_simt(h, q_lat, pool, n_pool_blocks, block_table, max_blocks, seq_lens,
+                                         cu_q, batch, n_tok, o_lat, lse, stream));
+  }
+  return MLA_OK;
+}
+
+// ---------------------------------------------------------------- a5
+size_t mla_out_workspace_bytes(const mla_handle* h, int n_tok) {
+  if (!h || n_tok < 0) return 0;
+  const size_t n = static_cast<size_t>(n_tok) * h->dims.n_h * h->dims.d_h * elem_bytes(h);
+  return (n + 255) & ~static_cast<size_t>(255);
+}
+
+mla_status mla_out(mla_handle* h, const void* o_lat, const void* w_uv, const void* w_o, int n_tok, void* u,
+                   void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!h || n_tok < 0) return MLA_ERR_INVALID_ARG;
+  if (n_tok == 0) return MLA_OK;
+  for (const void* p : {o_lat, w_uv, w_o, static_cast<const void*>(u)})
+    if (!p || !aligned16(p)) return MLA_ERR_INVALID_ARG;
+  if (!ws || !aligned16(ws) || ws_bytes < mla_out_workspace_bytes(h, n_tok)) return MLA_ERR_WORKSPACE;
+  const mla_dims& d = h->dims;
+  const int H = d.n_h * d.d_h;
+  MLA_TRY_CUDA(mla::launch_up_project_simt(h, o_lat, w_uv, n_tok, ws, stream));
+  MLA_TRY_CUDA(mla::launch_linear(h, ws, H, w_o, H, d.d_model, u, d.d_model, n_tok, stream));
+  return MLA_OK;
+}
+
+// ---------------------------------------------------------------- status
+mla_status mla_check_device_status(mla_handle* h, cudaStream_t stream) {
+  if (!h) return MLA_ERR_INVALID_ARG;
+  MLA_TRY_CUDA(cudaStreamSynchronize(stream));
+  int v = 0;
+  MLA_TRY_CUDA(cudaMemcpy(&v, h->status, sizeof(int), cudaMemcpyDeviceToHost));
+  MLA_TRY_CUDA(cudaMemset(h->status, 0, sizeof(int)));
+  return static_cast<mla_status>(v);
+}
+
+mla_status mla_selftest_wait_timeout(mla_handle* h, cudaStream_t stream) {
+  if (!h) return MLA_ERR_INVALID_ARG;
+  MLA_TRY_CUDA(mla::launch_wait_timeout_selftest(h, stream));
+  return MLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,225 @@
+"""ctypes binding of libmla.so (include/mla.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors (PyTorch provides device memory and
+streams); their data pointers and the current stream are passed through.
+There is no CPU fallback: without the built library, or without a CUDA
+device, these calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+from .build import LIB, ROOT
+from .synth import Dims
+
+HEADER = os.path.join(ROOT, "include", "mla.h")
+
+MLA_OK = 0
+STATUS = {
+    0: "MLA_OK",
+    1: "MLA_ERR_INVALID_ARG",
+    2: "MLA_ERR_UNSUPPORTED",
+    3: "MLA_ERR_WORKSPACE",
+    4: "MLA_ERR_CUDA",
+    5: "MLA_ERR_DEVICE_TIMEOUT",
+    6: "MLA_ERR_DEVICE_BOUNDS",
+}
+BF16, F32 = 0, 1
+
+
+class MLAError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class _Dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("n_h", "d_h", "d_hr", "d_c", "d_cq", "d_model", "block")] + [
+        ("rope_base", ctypes.c_float), ("scale", ctypes.c_float), ("dtype", ctypes.c_int)]
+
+
+_lib = None
+P, I, SZ, LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_longlong
+
+_SIGS = {
+    "mla_create": (I, [ctypes.POINTER(_Dims), I, ctypes.POINTER(P)]),
+    "mla_destroy": (None, [P]),
+    "mla_status_string": (ctypes.c_char_p, [I]),
+    "mla_num_sms": (I, [P]),
+    "mla_uses_tensor_path": (I, [P]),
+    "mla_set_wait_limit": (I, [P, LL]),
+    "mla_q_proj_workspace_bytes": (SZ, [P, I]),
+    "mla_q_proj": (I, [P, P, P, P, P, I, P, P, P, SZ, P]),
+    "mla_cache_append": (I, [P, P, P, P, P, I, P, I, I, P, I, P]),
+    "mla_absorb_q": (I, [P, P, P, P, I, P, P, P]),
+    "mla_decode_workspace_bytes": (SZ, [P, I, I]),
+    "mla_decode": (I, [P, P, P, I, P, I, P, P, I, I, I, P, SZ, P, P, P]),
+    "mla_out_workspace_bytes": (SZ, [P, I]),
+    "mla_out": (I, [P, P, P, P, I, P, P, SZ, P]),
+    "mla_check_device_status": (I, [P, P]),
+    "mla_selftest_wait_timeout": (I, [P, P]),
+}
+
+
+def header_symbols() -> list:
+    """Every function name declared in include/mla.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(mla_\w+)\s*\(", text, re.M)))
+
+
+def load(path: str = LIB):
+    """Load libmla.so and declare its signatures (no GPU needed)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with head_latent_attention_26_b300.build.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check(code: int, what: str):
+    if code != MLA_OK:
+        raise MLAError(code, what)
+
+
+class MLA:
+    """One attention layer's kernels on the current CUDA device.
+
+    dims: layer sizes; max_pos: positions the RoPE table covers; dtype:
+    torch.bfloat16 (storage and MMA type) or torch.float32.
+    """
+
+    def __init__(self, dims: Dims, max_pos: int, dtype=torch.bfloat16):
+        if not torch.cuda.is_available():
+            raise RuntimeError("MLA needs a CUDA device: there is no CPU fallback")
+        self.lib = load()
+        self.dims = dims
+        self.dtype = dtype
+        self.max_pos = max_pos
+        d = _Dims(dims.n_h, dims.d_h, dims.d_hr, dims.d_c, dims.d_cq, dims.d_model, dims.block,
+                  dims.rope_base, dims.scale, BF16 if dtype == torch.bfloat16 else F32)
+        h = P()
+        _check(self.lib.mla_create(ctypes.byref(d), max_pos, ctypes.byref(h)), "mla_create")
+        self.h = h
+        self._ws = {}
+
+    def __del__(self):
+        h = getattr(self, "h", None)
+        if h:
+            self.lib.mla_destroy(h)
+            self.h = None
+
+    # ---- plumbing ---------------------------------------------------------
+    @property
+    def tensor_path(self) -> bool:
+        return bool(self.lib.mla_uses_tensor_path(self.h))
+
+    @property
+    def num_sms(self) -> int:
+        return self.lib.mla_num_sms(self.h)
+
+    def workspace(self, key: str, nbytes: int) -> torch.Tensor:
+        """A cached device buffer of at least nbytes (allocated by torch)."""
+        buf = self._ws.get(key)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+            self._ws[key] = buf
+        return buf
+
+    def set_wait_limit(self, polls: int):
+        _check(self.lib.mla_set_wait_limit(self.h, polls), "mla_set_wait_limit")
+
+    def check(self):
+        """Synchronise and raise if any kernel recorded a device-side error."""
+        _check(self.lib.mla_check_device_status(self.h, P(_stream())), "device status")
+
+    def device_status(self) -> int:
+        return self.lib.mla_check_device_status(self.h, P(_stream()))
+
+    def selftest_wait_timeout(self) -> int:
+        _check(self.lib.mla_selftest_wait_timeout(self.h, P(_stream())), "selftest launch")
+        return self.device_status()
+
+    # ---- the path ---------------------------------------------------------
+    def q_proj(self, x, W_dq, W_uq, W_qr, q_c=None, q_r=None):
+        d, n = self.dims, x.shape[0]
+        q_c = torch.empty(n, d.n_h, d.d_h, dtype=self.dtype, device=x.device) if q_c is None else q_c
+        q_r = torch.empty(n, d.n_h, d.d_hr, dtype=self.dtype, device=x.device) if q_r is None else q_r
+        nb = self.lib.mla_q_proj_workspace_bytes(self.h, n)
+        ws = self.workspace("q_proj", nb)
+        _check(self.lib.mla_q_proj(self.h, _ptr(x), _ptr(W_dq), _ptr(W_uq), _ptr(W_qr), n, _ptr(q_c), _ptr(q_r),
+                                   _ptr(ws), ws.numel(), P(_stream())), "mla_q_proj")
+        return q_c, q_r
+
+    def cache_append(self, x, W_dkr, seq_idx, pos, block_table, pool):
+        _check(self.lib.mla_cache_append(self.h, _ptr(x), _ptr(W_dkr), _ptr(seq_idx), _ptr(pos), x.shape[0],
+                                         _ptr(block_table), block_table.shape[1], block_table.shape[0],
+                                         _ptr(pool), pool.shape[0], P(_stream())), "mla_cache_append")
+        return pool
+
+    def absorb_q(self, q_c, q_r, pos, W_uk, q_lat=None):
+        d, n = self.dims, q_c.shape[0]
+        q_lat = torch.empty(n, d.n_h, d.width, dtype=self.dtype, device=q_c.device) if q_lat is None else q_lat
+        _check(self.lib.mla_absorb_q(self.h, _ptr(q_c), _ptr(q_r), _ptr(pos), n, _ptr(W_uk), _ptr(q_lat),
+                                     P(_stream())), "mla_absorb_q")
+        return q_lat
+
+    def decode_workspace_bytes(self, n_tok: int, num_workers: int = 0) -> int:
+        return self.lib.mla_decode_workspace_bytes(self.h, n_tok, num_workers)
+
+    def decode(self, q_lat, pool, block_table, seq_lens, cu_q, num_workers: int = 0, o_lat=None, lse=None,
+               ws=None):
+        d, n = self.dims, q_lat.shape[0]
+        o_lat = torch.empty(n, d.n_h, d.d_c, dtype=self.dtype, device=q_lat.device) if o_lat is None else o_lat
+        lse = torch.empty(n, d.n_h, dtype=torch.float32, device=q_lat.device) if lse is None else lse
+        if ws is None:
+            ws = self.workspace("decode", self.decode_workspace_bytes(n, num_workers))
+        _check(self.lib.mla_decode(self.h, _ptr(q_lat), _ptr(pool), pool.shape[0], _ptr(block_table),
+                                   block_table.shape[1], _ptr(seq_lens), _ptr(cu_q), seq_lens.shape[0], n,
+                                   num_workers, _ptr(ws), ws.numel(), _ptr(o_lat), _ptr(lse), P(_stream())),
+               "mla_decode")
+        return o_lat, lse
+
+    def out(self, o_lat, W_uv, W_o, u=None):
+        d, n = self.dims, o_lat.shape[0]
+        u = torch.empty(n, d.d_model, dtype=self.dtype, device=o_lat.device) if u is None else u
+        ws = self.workspace("out", self.lib.mla_out_workspace_bytes(self.h, n))
+        _check(self.lib.mla_out(self.h, _ptr(o_lat), _ptr(W_uv), _ptr(W_o), n, _ptr(u), _ptr(ws), ws.numel(),
+                                P(_stream())), "mla_out")
+        return u
+
+    def decode_step(self, x, W: dict, W_dkr, seq_idx, pos, block_table, pool, seq_lens, cu_q,
+                    num_workers: int = 0, out: dict | None = None):
+        """One whole decode step for new tokens x: project the query, append
+        the new cache rows, absorb W^UK, attend over the latent cache and
+        project the output.  Returns u [n_tok, d_model]."""
+        out = {} if out is None else out
+        q_c, q_r = self.q_proj(x, W["W_dq"], W["W_uq"], W["W_qr"], out.get("q_c"), out.get("q_r"))
+        self.cache_append(x, W_dkr, seq_idx, pos, block_table, pool)
+        q_lat = self.absorb_q(q_c, q_r, pos, W["W_uk"], out.get("q_lat"))
+        o_lat, lse = self.decode(q_lat, pool, block_table, seq_lens, cu_q, num_workers, out.get("o_lat"),
+                                 out.get("lse"))
+        u = self.out(o_lat, W["W_uv"], W["W_o"], out.get("u"))
+        out.update(q_c=q_c, q_r=q_r, q_lat=q_lat, o_lat=o_lat, lse=lse, u=u)
+        return u
