@@ -743,3 +743,83 @@ cudaError_t launch_wait_timeout_selftest(const mla_handle* h, cudaStream_t s) {
   return cudaGetLastError();
 }
 }  // namespace mla
+
+// ---------------------------------------------------------------------------
+// Decode without caller-provided workspace.
+//
+// Some callers cannot allocate device memory at call time: a plugin hosted by
+// a serving engine that has reserved the whole device-memory budget up front
+// and hands the plugin no allocator, or a latency-critical loop that must not
+// call cudaMalloc because it can synchronise the device and take unbounded
+// time.  For them the split-KV scratch (token prefix sums and per-worker
+// partial outputs) lives in the fixed array below, which every device that
+// loads this library keeps until the process exits.
+// ---------------------------------------------------------------------------
+namespace mla {
+namespace {
+constexpr int kNoAllocMaxTokens = 8192;
+constexpr int kNoAllocMaxWorkers = 32;
+constexpr size_t kNoAllocPrefixBytes = (sizeof(int) * (kNoAllocMaxTokens + 1) + 255) & ~static_cast<size_t>(255);
+constexpr size_t kNoAllocPartOBytes = sizeof(float) * 2 * kNoAllocMaxWorkers * kHeads * kDc;
+constexpr size_t kNoAllocPartLseBytes = sizeof(float) * 2 * kNoAllocMaxWorkers * kHeads;
+constexpr size_t kNoAllocScratchBytes = kNoAllocPrefixBytes + kNoAllocPartOBytes + kNoAllocPartLseBytes;
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+void* g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+
+size_t decode_noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
+int decode_noalloc_max_tokens() { return kNoAllocMaxTokens; }
+int decode_noalloc_max_workers() { return kNoAllocMaxWorkers; }
+
+// 0 = ok, 1 = sizes beyond the fixed scratch, 2 = CUDA error.
+int launch_decode_tc_noalloc(const mla_handle* h, const void* q_lat, const void* pool, int n_pool_blocks,
+                             const int* block_table, int max_blocks, const int* seq_lens, const int* cu_q,
+                             int batch, int n_tok, int num_workers, void* o_lat, float* lse, cudaStream_t s) {
+  const int W = num_workers > 0 ? num_workers : min(max(1, h->num_sms / 2), kNoAllocMaxWorkers);
+  if (n_tok > kNoAllocMaxTokens || W > kNoAllocMaxWorkers) return 1;
+  // Once per device, with that device current: the device address of the
+  // scratch array (its host-side name is only a stand-in for it).
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 2;
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return 2;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  Maps maps;
+  const long long rows = static_cast<long long>(n_pool_blocks) * kTile;
+  if (!encode_pool_map(&maps.latent, pool, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_pool_map(&maps.rope, pool, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return 2;
+  uint8_t* w = static_cast<uint8_t*>(g_noalloc_ptr[dev]);
+  Params prm;
+  prm.prefix = reinterpret_cast<int*>(w);
+  prm.part_o = reinterpret_cast<float*>(w + kNoAllocPrefixBytes);
+  prm.part_lse = reinterpret_cast<float*>(w + kNoAllocPrefixBytes + kNoAllocPartOBytes);
+  prm.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
+  prm.block_table = block_table;
+  prm.seq_lens = seq_lens;
+  prm.cu_q = cu_q;
+  prm.o_lat = static_cast<__nv_bfloat16*>(o_lat);
+  prm.lse = lse;
+  prm.status = h->status;
+  prm.wait_limit = h->wait_limit;
+  prm.max_blocks = max_blocks;
+  prm.batch = batch;
+  prm.n_tok = n_tok;
+  prm.n_pool_blocks = n_pool_blocks;
+  prm.workers = W;
+  prm.scale_log2 = h->dims.scale * kLog2e;
+  plan_kernel<<<1, 1024, 0, s>>>(seq_lens, cu_q, batch, n_tok, max_blocks, const_cast<int*>(prm.prefix), h->status);
+  if (cudaGetLastError() != cudaSuccess) return 2;
+  if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+    return 2;
+  decode_tc_kernel<<<2 * W, kThreads, kSmemBytes, s>>>(maps, prm);
+  if (cudaGetLastError() != cudaSuccess) return 2;
+  combine_kernel<<<dim3(n_tok, 2), 256, 0, s>>>(prm.prefix, n_tok, W, prm.part_o, prm.part_lse, prm.o_lat, lse);
+  return cudaGetLastError() == cudaSuccess ? 0 : 2;
+}
+}  // namespace mla

@@ -84,4 +84,11 @@ cudaError_t launch_decode_tc(const mla_handle* h, const void* q_lat, const void*
                              const int* seq_lens, const int* cu_q, int batch, int n_tok,
                              int num_workers, void* ws, size_t ws_bytes, void* o_lat, float* lse,
                              cudaStream_t s);
+// Same kernels with their scratch in a fixed device array (no allocation).
+int launch_decode_tc_noalloc(const mla_handle* h, const void* q_lat, const void* pool, int n_pool_blocks,
+                             const int* block_table, int max_blocks, const int* seq_lens, const int* cu_q,
+                             int batch, int n_tok, int num_workers, void* o_lat, float* lse, cudaStream_t s);
+size_t decode_noalloc_scratch_bytes();
+int decode_noalloc_max_tokens();
+int decode_noalloc_max_workers();
 }  // namespace mla

@@ -190,6 +190,29 @@ mla_status mla_decode(mla_handle* h, const void* q_lat, const void* pool, int n_
   return MLA_OK;
 }
 
+// ---------------------------------------------------------------- a3 + a4, fixed scratch
+mla_status mla_decode_noalloc(mla_handle* h, const void* q_lat, const void* pool, int n_pool_blocks,
+                              const int* block_table, int max_blocks, const int* seq_lens, const int* cu_q,
+                              int batch, int n_tok, int num_workers, void* o_lat, float* lse,
+                              cudaStream_t stream) {
+  if (!h || n_tok < 0 || batch < 0 || num_workers < 0) return MLA_ERR_INVALID_ARG;
+  if (n_tok == 0) return MLA_OK;
+  if (batch < 1 || max_blocks < 1 || n_pool_blocks < 1) return MLA_ERR_INVALID_ARG;
+  for (const void* p : {q_lat, pool, static_cast<const void*>(o_lat), static_cast<const void*>(lse)})
+    if (!p || !aligned16(p)) return MLA_ERR_INVALID_ARG;
+  for (const int* p : {block_table, seq_lens, cu_q})
+    if (!p || !aligned4(p)) return MLA_ERR_INVALID_ARG;
+  if (!h->tensor_path) {  // the generic kernels need no scratch at all
+    MLA_TRY_CUDA(mla::launch_decode_simt(h, q_lat, pool, n_pool_blocks, block_table, max_blocks, seq_lens,
+                                         cu_q, batch, n_tok, o_lat, lse, stream));
+    return MLA_OK;
+  }
+  const int r = mla::launch_decode_tc_noalloc(h, q_lat, pool, n_pool_blocks, block_table, max_blocks, seq_lens,
+                                              cu_q, batch, n_tok, num_workers, o_lat, lse, stream);
+  if (r == 1) return MLA_ERR_WORKSPACE;
+  return r == 0 ? MLA_OK : MLA_ERR_CUDA;
+}
+
 // ---------------------------------------------------------------- a5
 size_t mla_out_workspace_bytes(const mla_handle* h, int n_tok) {
   if (!h || n_tok < 0) return 0;

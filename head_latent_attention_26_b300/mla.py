@@ -60,6 +60,7 @@ _SIGS = {
     "mla_absorb_q": (I, [P, P, P, P, I, P, P, P]),
     "mla_decode_workspace_bytes": (SZ, [P, I, I]),
     "mla_decode": (I, [P, P, P, I, P, I, P, P, I, I, I, P, SZ, P, P, P]),
+    "mla_decode_noalloc": (I, [P, P, P, I, P, I, P, P, I, I, I, P, P, P]),
     "mla_out_workspace_bytes": (SZ, [P, I]),
     "mla_out": (I, [P, P, P, P, I, P, P, SZ, P]),
     "mla_check_device_status": (I, [P, P]),
@@ -199,6 +200,18 @@ class MLA:
                                    block_table.shape[1], _ptr(seq_lens), _ptr(cu_q), seq_lens.shape[0], n,
                                    num_workers, _ptr(ws), ws.numel(), _ptr(o_lat), _ptr(lse), P(_stream())),
                "mla_decode")
+        return o_lat, lse
+
+    def decode_noalloc(self, q_lat, pool, block_table, seq_lens, cu_q, num_workers: int = 0, o_lat=None,
+                       lse=None):
+        """mla_decode_noalloc: the same attention, scratch in the library's
+        fixed device array instead of a workspace argument."""
+        d, n = self.dims, q_lat.shape[0]
+        o_lat = torch.empty(n, d.n_h, d.d_c, dtype=self.dtype, device=q_lat.device) if o_lat is None else o_lat
+        lse = torch.empty(n, d.n_h, dtype=torch.float32, device=q_lat.device) if lse is None else lse
+        _check(self.lib.mla_decode_noalloc(self.h, _ptr(q_lat), _ptr(pool), pool.shape[0], _ptr(block_table),
+                                           block_table.shape[1], _ptr(seq_lens), _ptr(cu_q), seq_lens.shape[0], n,
+                                           num_workers, _ptr(o_lat), _ptr(lse), P(_stream())), "mla_decode_noalloc")
         return o_lat, lse
 
     def out(self, o_lat, W_uv, W_o, u=None):

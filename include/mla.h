@@ -156,6 +156,34 @@ mla_status mla_decode(mla_handle* h, const void* q_lat, const void* pool, int n_
                       const int* cu_q, int batch, int n_tok, int num_workers, void* ws,
                       size_t ws_bytes, void* o_lat, float* lse, cudaStream_t stream);
 
+/* ---- decode without a workspace argument ------------------------------------
+ * The pages have no counterpart to this call; it is a convenience of this
+ * library.  It computes exactly what mla_decode computes, for callers that
+ * cannot allocate device memory when they call: for example a plugin whose
+ * host serving engine has reserved the whole device-memory budget and offers
+ * it no allocator, or a latency-critical loop that must not call cudaMalloc
+ * because that call can synchronise the device and take unbounded time.
+ *
+ * Its split-KV scratch is one fixed array in device memory (16,843,008 bytes
+ * on the tensor path), created when the library is loaded and kept by every
+ * device that loads it until the process exits.  Limits: n_tok <= 8192 and
+ * at most 32 workers (num_workers = 0 picks min(SMs/2, 32)); larger requests
+ * return MLA_ERR_WORKSPACE without launching.  Layer sizes outside the tensor
+ * path need no scratch and run the generic kernels.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Every
+ * call shares the one array: calls whose kernels overlap on the GPU (other
+ * streams, other threads, other handles of the same device) race on it and
+ * must be serialised by the caller.  Nothing in the array needs to start at
+ * zero; each call writes every scratch byte it later reads.
+ * This call allocates nothing and frees nothing.  Arguments and outputs are
+ * those of mla_decode. */
+mla_status mla_decode_noalloc(mla_handle* h, const void* q_lat, const void* pool, int n_pool_blocks,
+                              const int* block_table, int max_blocks, const int* seq_lens,
+                              const int* cu_q, int batch, int n_tok, int num_workers, void* o_lat,
+                              float* lse, cudaStream_t stream);
+
 /* ---- a5: output ------------------------------------------------------------
  * o_i = W^UV_i o~_i ([kasblo] "V側は、小さな表現の加重和を先に求める") and
  * u = W^O [o_1; ...; o_n_h] ([qiita] "Attention 計算").
