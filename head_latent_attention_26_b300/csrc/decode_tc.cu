@@ -8,18 +8,27 @@
 // dimension of every MMA, each 64-row cache block is one key tile.
 //
 // Layout of the work (fixed sizes: n_h = 128, d_c = 512, d_hr = 64, block = 64):
-// * A worker is a cluster of two CTAs.  CTA c owns latent columns
-//   [256c, 256c+256) and RoPE columns [512+32c, 512+32c+32) of every cached
-//   row; it TMA-loads only those 288 columns of each key tile (36 KB).
+// * A worker is a cluster of two CTAs.  The fp32 accumulator O for 128 heads x
+//   512 latent columns fills one SM's TMEM, so it is split by columns: CTA c
+//   owns latent columns [256c, 256c+256) and RoPE columns [512+32c, +32) of
+//   every cached row and TMA-loads only those 288 columns of each tile (36 KB).
 // * Scores: CTA c computes the partial score over its 288 columns,
-//   S_c = Q~[:, own] . C[:, own]^T  (M=128, N=64, K=288), with the latent part
-//   of Q~ resident in TMEM (A operand) and its RoPE part in shared memory.
-// * The two partial score tiles are swapped through distributed shared memory;
-//   both CTAs add them (fp32, commutative, so bit-identical) and run the same
-//   online softmax, so no softmax state needs to be exchanged.
+//   S_c = Q~[:, own] . C[:, own]^T  (M=128, N=64, K=288), with its half of the
+//   latent query (latent and RoPE parts) resident in TMEM as the A operand.
+// * Each row warp (32 heads) ships its 32 x 64 block of partial scores, scaled
+//   to log2 units and rounded to fp16, straight from registers into the same
+//   warp's inbox in the peer CTA with st.async (completion counted on the
+//   peer's mbarrier, no fence), one tile ahead of the tile it combines, so the
+//   exchange hides behind a tile of work.  Both CTAs add the two fp16
+//   partials in fp32 (the sum commutes, so both get bit-identical scores) and
+//   run the same online softmax: no softmax state is exchanged.
 // * Values: CTA c accumulates O[:, own 256 latent columns] += P . C[:, own]
-//   (M=128, N=256, K=64) in TMEM, reading the same shared-memory key tile as
-//   an MN-major B operand.  No K or V is ever expanded.
+//   (M=128, N=256, K=64) in TMEM, with P (bf16) in TMEM and the key tile read
+//   again from the same shared-memory stage as an MN-major B operand.  No K or
+//   V is ever expanded.
+// * The MMA issuer computes S two tiles ahead of the softmax: while the row
+//   warps turn tile t into probabilities they hold S(t+1) in registers and the
+//   tensor pipe runs O(t-1) and S(t+2) (one TMEM buffer for S is enough).
 // * Rescaling of O is lazy: the running max only moves when a tile's max
 //   exceeds it by more than 2^8, which keeps every exp2 argument <= 8 and the
 //   result exact (numerator and denominator share the stale max).
@@ -34,6 +43,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -46,21 +56,22 @@ namespace {
 
 constexpr int kHeads = 128;
 constexpr int kTile = 64;               // keys per tile = rows per cache block
+constexpr int kBlockRows = 64;
 constexpr int kWidth = 576;             // d_c + d_hr
 constexpr int kDc = 512;
-constexpr int kStages = 4;
-constexpr uint32_t kBoxBytes = 64 * 128;                    // 64 keys x 64 cols bf16
-constexpr uint32_t kRopeBoxBytes = 64 * 64;                 // 64 keys x 32 cols bf16
+constexpr int kStages = 5;
+constexpr uint32_t kBoxBytes = kTile * 128;                 // 64 keys x 64 cols bf16 (128B swizzle)
+constexpr uint32_t kRopeBoxBytes = kTile * 64;              // 64 keys x 32 cols bf16 (64B swizzle)
 constexpr uint32_t kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;  // 36864
-constexpr uint32_t kQRopeBytes = kHeads * 64;               // 128 heads x 32 cols bf16
-constexpr uint32_t kInboxBytes = kHeads * 256;              // 128 heads x 64 fp32
+constexpr uint32_t kXBlockBytes = 32 * kTile * 2;           // one warp's 32 heads x 64 keys fp16
+constexpr uint32_t kXSlotBytes = 4 * kXBlockBytes;          // all four row warps
 constexpr uint32_t kOffStages = 0;
-constexpr uint32_t kOffQRope = kOffStages + kStages * kStageBytes;
-constexpr uint32_t kOffInbox = kOffQRope + kQRopeBytes;
-constexpr uint32_t kOffBars = kOffInbox + 2 * kInboxBytes;
-constexpr uint32_t kSmemBytes = kOffBars + 256 + 1024;      // + alignment slack
-// TMEM columns (512 allocated): O half | S partial | Q~ latent half | P
-constexpr uint32_t kTmemO = 0, kTmemS = 256, kTmemQ = 320, kTmemP = 448;
+constexpr uint32_t kOffInbox = kOffStages + kStages * kStageBytes;
+constexpr uint32_t kOffBars = kOffInbox + 2 * kXSlotBytes;
+constexpr uint32_t kSmemBytes = kOffBars + 512 + 1024;      // + alignment slack
+// TMEM columns (512 allocated): O half | Q~ latent half | Q~ RoPE half | P | S
+// (bf16 operands hold two elements per 32-bit column)
+constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemQR = 384, kTmemP = 416, kTmemS = 448;
 constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -88,12 +99,15 @@ struct Params {
 
 struct Bars {
   uint64_t full[kStages], empty[kStages];
-  uint64_t q_ready, s_full, s_free, p_ready, o_done;
-  uint64_t xin_full[2], xout_free[2];
+  uint64_t q_ready, s_full, s_free, p_ready, p_free;
+  uint64_t xin_full[2][4];    // peer warp w's partial scores landed in inbox slot
+  uint64_t inbox_free[2][4];  // peer warp w has consumed the slot this CTA writes into
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(Bars) <= 512, "barrier block");
+constexpr uint32_t kBarSlot = 4 * sizeof(uint64_t);  // stride of one slot in the [2][4] barrier arrays
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Params& p, Bars* bs,
                                          bool cluster_scope = false) {
@@ -163,6 +177,14 @@ __device__ __forceinline__ UnitIter make_iter(const Params& p, int g) {
   return it;
 }
 
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float2 unpack_half2(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -182,21 +204,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bs->s_full, 1);
     mbar_init(&bs->s_free, 4);
     mbar_init(&bs->p_ready, 4);
-    mbar_init(&bs->o_done, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bs->xin_full[s], 128);
-      mbar_init(&bs->xout_free[s], 128);
-    }
+    mbar_init(&bs->p_free, 1);
+    for (int s = 0; s < 2; ++s)
+      for (int w = 0; w < 4; ++w) {
+        mbar_init(&bs->xin_full[s][w], 1);
+        mbar_init(&bs->inbox_free[s][w], 1);
+      }
     mbar_init(&bs->drain, 1);
     bs->abort = 0;
     fence_mbar_init();
+    // first phase of every inbox barrier: one arrival (this one) + the bytes
+    for (int s = 0; s < 2; ++s)
+      for (int w = 0; w < 4; ++w) mbar_arrive_expect_tx(&bs->xin_full[s][w], kXBlockBytes);
   }
   if (warp == 1) {
     tmem_alloc(&bs->tmem_base, 512);
     tmem_relinquish();
   }
   __syncthreads();
-  cluster_arrive();  // peer barriers are initialised before any remote arrive
+  cluster_arrive();  // peer barriers are initialised before any remote access
   cluster_wait();
   tc_fence_after();
   const uint32_t tmem = bs->tmem_base;
@@ -206,6 +232,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&maps.latent);
       tma_prefetch_desc(&maps.rope);
+      const uint64_t pol = l2_policy_evict_first();  // every cache row is read once
       UnitIter iter = make_iter(p, g);
       Unit u;
       uint32_t it = 0;
@@ -222,10 +249,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           uint8_t* st = smem + kOffStages + s * kStageBytes;
           mbar_arrive_expect_tx(&bs->full[s], kStageBytes);
-          const int y = blk * kTile;
+          const int y = blk * kBlockRows;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) tma_load_2d(st + j * kBoxBytes, &maps.latent, &bs->full[s], 256 * c + 64 * j, y);
-          tma_load_2d(st + 4 * kBoxBytes, &maps.rope, &bs->full[s], 512 + 32 * c, y);
+          for (int j = 0; j < 4; ++j)
+            tma_load_2d_hint(st + j * kBoxBytes, &maps.latent, &bs->full[s], 256 * c + 64 * j, y, pol);
+          tma_load_2d_hint(st + 4 * kBoxBytes, &maps.rope, &bs->full[s], 512 + 32 * c, y, pol);
         }
       }
       // drain: every issued stage must land before the CTA may exit
@@ -238,14 +266,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
+      const uint32_t idesc_s = idesc_bf16_f32(128, kTile, false, false);
       const uint32_t idesc_o = idesc_bf16_f32(128, 256, false, true);
-      const uint32_t qrope = smem_u32(smem + kOffQRope);
       UnitIter iter = make_iter(p, g);
       Unit u;
-      uint32_t it = 0, n_units = 0, sfree_n = 0, pready_n = 0;
+      uint32_t n_sq = 0;     // S tiles issued (global); tile k sits in stage k % kStages
+      uint32_t n_o = 0;      // O MMAs issued (global)
+      uint32_t n_units = 0;
       bool ok = true;
-      auto issue_s = [&](uint32_t k) {
+      // S(k) into the single S buffer once the row warps have read S(k-1) out of it
+      auto issue_s = [&]() -> bool {
+        const uint32_t k = n_sq;
+        if (!wait_bar(&bs->full[k % kStages], (k / kStages) & 1, p, bs)) return false;
+        if (k >= 1 && !wait_bar(&bs->s_free, (k - 1) & 1, p, bs)) return false;
+        tc_fence_after();
         const uint32_t st = smem_u32(smem + kOffStages + (k % kStages) * kStageBytes);
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
@@ -254,45 +288,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
-          const uint64_t ad = smem_desc(qrope + kk * 32, 16, 512, kSwizzle64B);
           const uint64_t bd = smem_desc(st + 4 * kBoxBytes + kk * 32, 16, 512, kSwizzle64B);
-          mma_ss(tmem + kTmemS, ad, bd, idesc_s, 1);
+          mma_ts(tmem + kTmemS, tmem + kTmemQR + kk * 8, bd, idesc_s, 1);
         }
         mma_commit(&bs->s_full);
+        ++n_sq;
+        return true;
       };
       while (ok && iter.next(p, g, u)) {
         ok = wait_bar(&bs->q_ready, n_units & 1, p, bs);
         ++n_units;
         if (!ok) break;
         tc_fence_after();
-        const uint32_t it0 = it;
-        ok = wait_bar(&bs->full[it % kStages], (it / kStages) & 1, p, bs);
-        if (!ok) break;
-        tc_fence_after();
-        issue_s(it);
-        for (int t = u.ta; t < u.tb && ok; ++t, ++it) {
-          if (t + 1 < u.tb) {
-            ok = wait_bar(&bs->full[(it + 1) % kStages], ((it + 1) / kStages) & 1, p, bs) &&
-                 wait_bar(&bs->s_free, sfree_n & 1, p, bs);
-            ++sfree_n;
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(it + 1);
-          } else {
-            ++sfree_n;  // the last tile's drain completes before the next q_ready
-          }
-          ok = wait_bar(&bs->p_ready, pready_n & 1, p, bs);
-          ++pready_n;
-          if (!ok) break;
+        const uint32_t n = static_cast<uint32_t>(u.tb - u.ta), it0 = n_sq;
+        if (!(ok = issue_s())) break;
+        if (n > 1 && !(ok = issue_s())) break;
+        for (uint32_t t = 0; t < n && ok; ++t) {
+          if (t + 2 < n && !(ok = issue_s())) break;  // waits until the row warps hold S(t+1)
+          if (!(ok = wait_bar(&bs->p_ready, n_o & 1, p, bs))) break;
           tc_fence_after();
-          const uint32_t st = smem_u32(smem + kOffStages + (it % kStages) * kStageBytes);
+          const uint32_t st = smem_u32(smem + kOffStages + ((it0 + t) % kStages) * kStageBytes);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = smem_desc(st + ks * 2048, 8192, 1024, kSwizzle128B);
-            mma_ts(tmem + kTmemO, tmem + kTmemP + ks * 8, bd, idesc_o, (it > it0 || ks > 0) ? 1u : 0u);
+            const uint64_t bd = smem_desc(st + ks * 2048, kBoxBytes, 1024, kSwizzle128B);
+            mma_ts(tmem + kTmemO, tmem + kTmemP + ks * 8, bd, idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
           }
-          mma_commit(&bs->o_done);
-          mma_commit(&bs->empty[it % kStages]);
+          mma_commit(&bs->p_free);
+          mma_commit(&bs->empty[(it0 + t) % kStages]);
+          ++n_o;
         }
       }
       if (!ok) {
@@ -308,23 +331,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;           // head = TMEM lane
     const int tr = threadIdx.x - 64;       // 0..127 among the row warps
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    uint8_t* inbox = smem + kOffInbox;
-    const uint32_t inbox_local = smem_u32(inbox);
-    const uint32_t inbox_peer = map_to_rank(inbox_local, peer);
-    const uint32_t xin_full_peer[2] = {map_to_rank(smem_u32(&bs->xin_full[0]), peer),
-                                       map_to_rank(smem_u32(&bs->xin_full[1]), peer)};
-    const uint32_t xout_free_peer[2] = {map_to_rank(smem_u32(&bs->xout_free[0]), peer),
-                                        map_to_rank(smem_u32(&bs->xout_free[1]), peer)};
+    // this warp's 4 KB block of inbox slot s sits at inbox0 + s * kXSlotBytes,
+    // at the same offset in the peer; row = lane, 16-byte chunks XOR-swizzled
+    const uint8_t* const inbox0 = smem + kOffInbox + q * kXBlockBytes;
+    const uint32_t peer_row0 = map_to_rank(smem_u32(inbox0 + lane * 128), peer);
+    const uint32_t peer_xin0 = map_to_rank(smem_u32(&bs->xin_full[0][q]), peer);
+    const uint32_t peer_free0 = map_to_rank(smem_u32(&bs->inbox_free[0][q]), peer);
     UnitIter iter = make_iter(p, g);
     Unit u;
-    uint32_t it = 0, sfull_n = 0, odone_n = 0;
+    uint32_t n_s = 0;      // S tiles read out of TMEM (global)
+    uint32_t n_send = 0;   // partial blocks sent to the peer (= received from it)
+    uint32_t n_recv = 0;
+    uint32_t n_p = 0;      // P tiles written (global) = tile index for the stage ring
     bool ok = true;
+
+    // Reads S out of TMEM, scales it to log2 units, rounds it to fp16 (kept in
+    // `own`) and stores it into the peer's inbox.
+    auto send = [&](uint32_t* own) -> bool {
+      if (!wait_bar(&bs->s_full, n_s & 1, p, bs)) return false;
+      ++n_s;
+      tc_fence_after();
+      uint32_t v[64];
+      tmem_ld32(tmem + lane_base + kTmemS, v);
+      tmem_ld32(tmem + lane_base + kTmemS + 32, v + 32);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bs->s_free);
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        own[j] = pack_half2(__uint_as_float(v[2 * j]) * p.scale_log2, __uint_as_float(v[2 * j + 1]) * p.scale_log2);
+      const uint32_t slot = n_send & 1;
+      if (n_send >= 2 && !wait_bar(&bs->inbox_free[slot][q], ((n_send >> 1) - 1) & 1, p, bs, true)) return false;
+      const uint32_t dst = peer_row0 + slot * kXSlotBytes, bar = peer_xin0 + slot * kBarSlot;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        st_async_v4(dst + ((ch ^ (lane & 7)) * 16), make_uint4(own[4 * ch], own[4 * ch + 1], own[4 * ch + 2], own[4 * ch + 3]),
+                    bar);
+      ++n_send;
+      return true;
+    };
+
     while (ok && iter.next(p, g, u)) {
-      // ---- latent query: own 256 latent columns -> TMEM, own 32 RoPE columns -> smem
+      // ---- latent query: own 256 latent + 32 RoPE columns of head r -> TMEM
       {
         const uint4* src = reinterpret_cast<const uint4*>(p.q_lat + (static_cast<size_t>(u.n) * kHeads + r) * kWidth + 256 * c);
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
+        for (int ch = 0; ch < 8; ++ch) {
           uint32_t v[16];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -332,80 +385,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             v[4 * j] = w.x; v[4 * j + 1] = w.y; v[4 * j + 2] = w.z; v[4 * j + 3] = w.w;
           }
           tmem_st16(tmem + lane_base + kTmemQ + ch * 16, v);
-          // second half of this 64-column chunk
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 w = __ldg(src + ch * 4 + 16 + j);
-            v[4 * j] = w.x; v[4 * j + 1] = w.y; v[4 * j + 2] = w.z; v[4 * j + 3] = w.w;
-          }
-          tmem_st16(tmem + lane_base + kTmemQ + 64 + ch * 16, v);
         }
         const uint4* rsrc = reinterpret_cast<const uint4*>(p.q_lat + (static_cast<size_t>(u.n) * kHeads + r) * kWidth + 512 + 32 * c);
-        uint8_t* qr = smem + kOffQRope + r * 64;
+        uint32_t v[16];
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) *reinterpret_cast<uint4*>(qr + ((ch ^ ((r >> 1) & 3)) * 16)) = __ldg(rsrc + ch);
+        for (int j = 0; j < 4; ++j) {
+          const uint4 w = __ldg(rsrc + j);
+          v[4 * j] = w.x; v[4 * j + 1] = w.y; v[4 * j + 2] = w.z; v[4 * j + 3] = w.w;
+        }
+        tmem_st16(tmem + lane_base + kTmemQR, v);
         tmem_st_wait();
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bs->q_ready);
       }
+      const int n = u.tb - u.ta;
+      uint32_t mine[32], nxt[32];
+      if (!(ok = send(mine))) break;
       float m = -INFINITY, l = 0.f;
-      for (int t = u.ta; t < u.tb && ok; ++t, ++it) {
-        const bool first = (t == u.ta);
-        // ---- 1. own partial scores out of TMEM
-        ok = wait_bar(&bs->s_full, sfull_n & 1, p, bs);
-        ++sfull_n;
-        if (!ok) break;
-        tc_fence_after();
+      for (int tt = 0; tt < n && ok; ++tt) {
+        const int t = u.ta + tt;
+        if (tt + 1 < n && !(ok = send(nxt))) break;
+        // ---- 1. the peer's partial scores of this tile: s = own + peer (log2 units)
         float s[64];
+        const uint32_t rslot = n_recv & 1;
         {
-          uint32_t v[16];
+          if (!(ok = wait_bar(&bs->xin_full[rslot][q], (n_recv >> 1) & 1, p, bs, true))) break;
+          ++n_recv;
+          if (lane == 0) mbar_arrive_expect_tx(&bs->xin_full[rslot][q], kXBlockBytes);  // arm the next phase
+          const uint8_t* row = inbox0 + rslot * kXSlotBytes + lane * 128;
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            tmem_ld16(tmem + lane_base + kTmemS + ch * 16, v);
-            tmem_ld_wait();
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint4 w = *reinterpret_cast<const uint4*>(row + ((ch ^ (lane & 7)) * 16));
+            const uint32_t pw[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int j = 0; j < 16; ++j) s[ch * 16 + j] = __uint_as_float(v[j]);
+            for (int e = 0; e < 4; ++e) {
+              const float2 a = unpack_half2(mine[4 * ch + e]), b = unpack_half2(pw[e]);
+              s[8 * ch + 2 * e] = a.x + b.x;
+              s[8 * ch + 2 * e + 1] = a.y + b.y;
+            }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bs->s_free);
-        // ---- 2. swap partial scores with the peer CTA
-        const uint32_t slot = it & 1;
-        if (it >= 2) {
-          ok = wait_bar(&bs->xout_free[slot], ((it >> 1) - 1) & 1, p, bs, true);
-          if (!ok) break;
-        }
-        {
-          const uint32_t dst = inbox_peer + slot * kInboxBytes + r * 256;
-#pragma unroll
-          for (int ch = 0; ch < 16; ++ch)
-            st_cluster_v4(dst + ((ch ^ (r & 15)) * 16), s[4 * ch], s[4 * ch + 1], s[4 * ch + 2], s[4 * ch + 3]);
-          mbar_arrive_cluster(xin_full_peer[slot]);
-        }
-        ok = wait_bar(&bs->xin_full[slot], (it >> 1) & 1, p, bs, true);
-        if (!ok) break;
-        {
-          const uint8_t* src = inbox + slot * kInboxBytes + r * 256;
-#pragma unroll
-          for (int ch = 0; ch < 16; ++ch) {
-            const float4 w = *reinterpret_cast<const float4*>(src + ((ch ^ (r & 15)) * 16));
-            s[4 * ch] += w.x; s[4 * ch + 1] += w.y; s[4 * ch + 2] += w.z; s[4 * ch + 3] += w.w;
-          }
-          mbar_arrive_cluster(xout_free_peer[slot]);
-        }
-        // ---- 3. online softmax in the log2 domain, causal mask on the last tile
+        // ---- 2. online softmax in the log2 domain, causal mask on the last tile
         const int valid = min(kTile, u.pos - t * kTile + 1);  // keys of this tile the token sees
         float mt = -INFINITY;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          s[j] = (j < valid) ? s[j] * p.scale_log2 : -INFINITY;
+          s[j] = (j < valid) ? s[j] : -INFINITY;
           mt = fmaxf(mt, s[j]);
         }
         float m_use = m, f = 1.f;
-        if (first) {
+        if (tt == 0) {
           m_use = mt;
         } else if (mt > m + kRescaleThreshold) {
           m_use = mt;
@@ -415,29 +445,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float rowsum = 0.f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(exp2f(s[2 * j] - m_use), exp2f(s[2 * j + 1] - m_use));
-          const float2 back = __bfloat1622float2(b2);
-          rowsum += back.x + back.y;
-          pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
+          const float e0 = exp2f(s[2 * j] - m_use), e1 = exp2f(s[2 * j + 1] - m_use);
+          rowsum += e0 + e1;
+          pk[j] = pack_bf16x2(e0, e1);
         }
-        l = first ? rowsum : l * f + rowsum;
+        l = (tt == 0) ? rowsum : l * f + rowsum;
         m = m_use;
-        // ---- 4. wait for the previous O MMA, rescale O if the max moved, write P
-        if (!first) {
-          ok = wait_bar(&bs->o_done, odone_n & 1, p, bs);
-          ++odone_n;
-          if (!ok) break;
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, f != 1.f)) {
+        // ---- 3. the previous O MMA is done (P is free); rescale O if the max moved; write P
+        if (n_p >= 1 && !(ok = wait_bar(&bs->p_free, (n_p - 1) & 1, p, bs))) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, f != 1.f)) {
 #pragma unroll 1
-            for (int ch = 0; ch < 16; ++ch) {
-              uint32_t v[16];
-              tmem_ld16(tmem + lane_base + kTmemO + ch * 16, v);
-              tmem_ld_wait();
+          for (int ch = 0; ch < 16; ++ch) {
+            uint32_t v[16];
+            tmem_ld16(tmem + lane_base + kTmemO + ch * 16, v);
+            tmem_ld_wait();
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * f);
-              tmem_st16(tmem + lane_base + kTmemO + ch * 16, v);
-            }
+            for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * f);
+            tmem_st16(tmem + lane_base + kTmemO + ch * 16, v);
           }
         }
         tmem_st16(tmem + lane_base + kTmemP, pk);
@@ -445,23 +470,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         // rows past the token's position may hold anything: zero them for the O MMA
         if (valid < kTile) {
-          uint8_t* st = smem + kOffStages + (it % kStages) * kStageBytes;
+          uint8_t* st = smem + kOffStages + (n_p % kStages) * kStageBytes;
           for (int idx = tr; idx < (kTile - valid) * 32; idx += 128) {
             const int row = valid + (idx >> 5), box = (idx >> 3) & 3, ch = idx & 7;
             *reinterpret_cast<uint4*>(st + box * kBoxBytes + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
           }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          asm volatile("bar.sync 1, 128;" ::: "memory");  // all four row warps zeroed their share
+          fence_proxy_async_smem();  // each warp's p_ready arrival covers its own share
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bs->p_ready);
+        if (lane == 0) {
+          mbar_arrive(&bs->p_ready);
+          mbar_arrive_relaxed_cluster(peer_free0 + rslot * kBarSlot);  // its values are consumed
+        }
+        ++n_p;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) mine[j] = nxt[j];
       }
       if (!ok) break;
       // ---- epilogue: O / l for this head and this CTA's 256 latent columns
-      ok = wait_bar(&bs->o_done, odone_n & 1, p, bs);
-      ++odone_n;
-      if (!ok) break;
+      if (!(ok = wait_bar(&bs->p_free, (n_p - 1) & 1, p, bs))) break;
       tc_fence_after();
       const float inv_l = 1.f / l;
       const float lse_val = (m + log2f(l)) * 0.69314718055994531f;
@@ -497,6 +525,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
     }
+    // a remote store into the peer must not outlive the peer: wait until the
+    // peer has consumed everything this warp sent (its inbox_free arrivals)
+    for (uint32_t k = (n_send > 2 ? n_send - 2 : 0); ok && k < n_send; ++k)
+      ok = wait_bar(&bs->inbox_free[k & 1][q], (k >> 1) & 1, p, bs, true);
   }
 
   __syncthreads();
@@ -524,9 +556,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ seq_
     if (n < n_tok) {
       const int b = seq_of_token(cu_q, batch, n);
       const int pos = __ldg(seq_lens + b) - (__ldg(cu_q + b + 1) - n);
-      if (pos < 0 || n < __ldg(cu_q + b) || n >= __ldg(cu_q + b + 1) || pos / kTile >= max_blocks) {
+      if (pos < 0 || n < __ldg(cu_q + b) || n >= __ldg(cu_q + b + 1) || pos / kBlockRows >= max_blocks) {
         report(status, MLA_ERR_DEVICE_BOUNDS);
-        tiles = pos >= 0 ? min(pos / kTile + 1, max_blocks) : 0;
+        tiles = pos >= 0 ? min(pos / kTile + 1, max_blocks * (kBlockRows / kTile)) : 0;
       } else {
         tiles = pos / kTile + 1;
       }
@@ -564,18 +596,12 @@ __device__ __forceinline__ int worker_of(long long x, int workers, int total) {
   return g;
 }
 
-// Partial slot that worker g wrote for token n: slot 2g when n is the token
-// its range starts in, else 2g+1; -1 for a worker with an empty range.
-__device__ __forceinline__ int piece_slot(const int* prefix, int n_tok, int workers, int total, int g, int n) {
-  int lo, hi;
-  worker_range(g, workers, total, lo, hi);
-  if (lo >= hi) return -1;
-  return 2 * g + (first_token_at(prefix, n_tok, lo) == n ? 0 : 1);
-}
-
 // Merge the pieces of every token whose keys were split across workers:
-// lse = ln sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s.  One warp per head;
-// the log-sum-exp over pieces is a warp-shuffle reduction.
+// lse = ln sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s (the standard
+// identity for a softmax split over disjoint key ranges; not on the pages).
+// One warp per (token, head); the pieces of a token are the workers g0..g1
+// whose ranges meet its tiles.  Worker g wrote slot 2g when its range starts
+// inside the token, else 2g+1 (its range started in an earlier token).
 __global__ void __launch_bounds__(256) combine_kernel(const int* __restrict__ prefix, int n_tok, int workers,
                                                       const float* __restrict__ part_o,
                                                       const float* __restrict__ part_lse,
@@ -587,63 +613,70 @@ __global__ void __launch_bounds__(256) combine_kernel(const int* __restrict__ pr
   const int g0 = worker_of(t0, workers, total), g1 = worker_of(t1 - 1, workers, total);
   if (g0 == g1) return;  // whole token inside one worker: already final
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * 8 + warp;
+  // lane k < npieces holds piece k's slot and lse
   const int npieces = g1 - g0 + 1;
-  for (int h = blockIdx.y * 8 + warp; h < kHeads; h += 8 * gridDim.y) {
-    // pass 1: L = ln sum exp(lse_s)
-    float mx = -INFINITY;
-    for (int k = lane; k < npieces; k += 32) {
-      const int slot = piece_slot(prefix, n_tok, workers, total, g0 + k, n);
-      if (slot >= 0) mx = fmaxf(mx, __ldg(part_lse + static_cast<size_t>(slot) * kHeads + h));
+  float mx = -INFINITY, my_lse = -INFINITY;
+  int my_slot = -1;
+  for (int k = lane; k < npieces; k += 32) {
+    const int g = g0 + k;
+    int lo, hi;
+    worker_range(g, workers, total, lo, hi);
+    int slot = -1;
+    if (lo < hi) slot = (k == 0 && lo < t0) ? 2 * g + 1 : 2 * g;
+    if (slot >= 0) {
+      const float v = __ldg(part_lse + static_cast<size_t>(slot) * kHeads + h);
+      mx = fmaxf(mx, v);
+      if (k < 32) { my_slot = slot; my_lse = v; }
     }
-    mx = warp_max(mx);
-    float sum = 0.f;
-    for (int k = lane; k < npieces; k += 32) {
-      const int slot = piece_slot(prefix, n_tok, workers, total, g0 + k, n);
-      if (slot >= 0) sum += expf(__ldg(part_lse + static_cast<size_t>(slot) * kHeads + h) - mx);
-    }
-    sum = warp_sum(sum);
-    const float L = mx + logf(sum);
-    // pass 2: weighted sum of the pieces, 16 columns per lane
-    float acc[16];
+  }
+  mx = warp_max(mx);
+  float sum = (my_slot >= 0) ? expf(my_lse - mx) : 0.f;
+  for (int k = lane + 32; k < npieces; k += 32) {  // more than 32 pieces: rare, recompute
+    const int g = g0 + k;
+    int lo, hi;
+    worker_range(g, workers, total, lo, hi);
+    if (lo < hi) sum += expf(__ldg(part_lse + static_cast<size_t>(2 * g) * kHeads + h) - mx);
+  }
+  sum = warp_sum(sum);
+  const float L = mx + logf(sum);
+  float acc[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-    for (int k = 0; k < npieces; ++k) {
-      const int slot = piece_slot(prefix, n_tok, workers, total, g0 + k, n);
-      if (slot < 0) continue;
-      const float w = expf(__ldg(part_lse + static_cast<size_t>(slot) * kHeads + h) - L);
-      const float4* src = reinterpret_cast<const float4*>(part_o + (static_cast<size_t>(slot) * kHeads + h) * kDc);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 v = __ldg(src + lane + 32 * j);
-        acc[4 * j] += w * v.x; acc[4 * j + 1] += w * v.y; acc[4 * j + 2] += w * v.z; acc[4 * j + 3] += w * v.w;
-      }
+  for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+  for (int k = 0; k < npieces; ++k) {
+    int slot;
+    float ls;
+    if (k < 32) {
+      slot = __shfl_sync(0xffffffffu, my_slot, k);
+      ls = __shfl_sync(0xffffffffu, my_lse, k);
+    } else {
+      const int g = g0 + k;
+      int lo, hi;
+      worker_range(g, workers, total, lo, hi);
+      slot = lo < hi ? 2 * g : -1;
+      ls = slot >= 0 ? __ldg(part_lse + static_cast<size_t>(slot) * kHeads + h) : -INFINITY;
     }
-    __nv_bfloat16* dst = o_lat + (static_cast<size_t>(n) * kHeads + h) * kDc;
+    if (slot < 0) continue;
+    const float w = expf(ls - L);
+    const float4* src = reinterpret_cast<const float4*>(part_o + (static_cast<size_t>(slot) * kHeads + h) * kDc);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int col = 4 * (lane + 32 * j);
-      reinterpret_cast<uint2*>(dst + col)[0] = make_uint2(pack_bf16x2(acc[4 * j], acc[4 * j + 1]),
-                                                          pack_bf16x2(acc[4 * j + 2], acc[4 * j + 3]));
+      const float4 v = __ldg(src + lane + 32 * j);
+      acc[4 * j] += w * v.x; acc[4 * j + 1] += w * v.y; acc[4 * j + 2] += w * v.z; acc[4 * j + 3] += w * v.w;
     }
-    if (lane == 0) lse[static_cast<size_t>(n) * kHeads + h] = L;
   }
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  __nv_bfloat16* dst = o_lat + (static_cast<size_t>(n) * kHeads + h) * kDc;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int col = 4 * (lane + 32 * j);
+    reinterpret_cast<uint2*>(dst + col)[0] = make_uint2(pack_bf16x2(acc[4 * j], acc[4 * j + 1]),
+                                                        pack_bf16x2(acc[4 * j + 2], acc[4 * j + 3]));
   }
-  return fn;
+  if (lane == 0) lse[static_cast<size_t>(n) * kHeads + h] = L;
 }
 
 bool encode_pool_map(CUtensorMap* m, const void* pool, long long rows, uint32_t box_cols, CUtensorMapSwizzle sw) {
-  auto enc = tensor_map_encoder();
+  auto enc = tma_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(kWidth), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(kWidth) * 2};
@@ -674,7 +707,7 @@ cudaError_t launch_decode_tc(const mla_handle* h, const void* q_lat, const void*
                              float* lse, cudaStream_t s) {
   const int W = resolve_workers(h, num_workers);
   Maps maps;
-  const long long rows = static_cast<long long>(n_pool_blocks) * kTile;
+  const long long rows = static_cast<long long>(n_pool_blocks) * kBlockRows;
   if (!encode_pool_map(&maps.latent, pool, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_pool_map(&maps.rope, pool, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
@@ -712,9 +745,10 @@ cudaError_t launch_decode_tc(const mla_handle* h, const void* q_lat, const void*
   decode_tc_kernel<<<2 * W, kThreads, kSmemBytes, s>>>(maps, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  combine_kernel<<<dim3(n_tok, 2), 256, 0, s>>>(prm.prefix, n_tok, W, prm.part_o, prm.part_lse, prm.o_lat, lse);
+  combine_kernel<<<dim3(n_tok, kHeads / 8), 256, 0, s>>>(prm.prefix, n_tok, W, prm.part_o, prm.part_lse, prm.o_lat, lse);
   return cudaGetLastError();
 }
+
 
 }  // namespace mla
 
@@ -790,7 +824,7 @@ int launch_decode_tc_noalloc(const mla_handle* h, const void* q_lat, const void*
     g_noalloc_ptr[dev] = ptr;
   }
   Maps maps;
-  const long long rows = static_cast<long long>(n_pool_blocks) * kTile;
+  const long long rows = static_cast<long long>(n_pool_blocks) * kBlockRows;
   if (!encode_pool_map(&maps.latent, pool, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_pool_map(&maps.rope, pool, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return 2;
@@ -819,7 +853,7 @@ int launch_decode_tc_noalloc(const mla_handle* h, const void* q_lat, const void*
     return 2;
   decode_tc_kernel<<<2 * W, kThreads, kSmemBytes, s>>>(maps, prm);
   if (cudaGetLastError() != cudaSuccess) return 2;
-  combine_kernel<<<dim3(n_tok, 2), 256, 0, s>>>(prm.prefix, n_tok, W, prm.part_o, prm.part_lse, prm.o_lat, lse);
+  combine_kernel<<<dim3(n_tok, kHeads / 8), 256, 0, s>>>(prm.prefix, n_tok, W, prm.part_o, prm.part_lse, prm.o_lat, lse);
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }
 }  // namespace mla

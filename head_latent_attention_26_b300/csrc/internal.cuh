@@ -2,6 +2,8 @@
 // the kernels of the library (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -17,7 +19,8 @@ struct mla_handle {
   float* rope_sin;
   int* status;      // first device-side error code, 0 = none
   long long wait_limit;
-  bool tensor_path;
+  bool tensor_path;  // tcgen05 decode serves these dims
+  bool proj_tc;      // tcgen05 projection kernels serve these dims
 };
 
 namespace mla {
@@ -84,6 +87,16 @@ cudaError_t launch_decode_tc(const mla_handle* h, const void* q_lat, const void*
                              const int* seq_lens, const int* cu_q, int batch, int n_tok,
                              int num_workers, void* ws, size_t ws_bytes, void* o_lat, float* lse,
                              cudaStream_t s);
+// cuTensorMapEncodeTiled from the driver (looked up once); null if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tma_encoder();
+// tcgen05 projections (bf16, d_h = 128, widths multiples of 64)
+cudaError_t launch_linear_tc(const mla_handle* h, const void* X, int x_cols, const void* W, int in, int out,
+                             int groups, int x_group_cols, void* Y, long long ldy, int n_tok, cudaStream_t s);
+cudaError_t launch_cache_append_tc(const mla_handle* h, const void* x, const void* w_dkr, const int* seq_idx,
+                                   const int* pos, int n_new, const int* block_table, int max_blocks, int batch,
+                                   void* pool, int n_pool_blocks, cudaStream_t s);
+cudaError_t launch_absorb_q_tc(const mla_handle* h, const void* q_c, const void* q_r, const int* pos, int n_tok,
+                               const void* w_uk, void* q_lat, cudaStream_t s);
 // Same kernels with their scratch in a fixed device array (no allocation).
 int launch_decode_tc_noalloc(const mla_handle* h, const void* q_lat, const void* pool, int n_pool_blocks,
                              const int* block_table, int max_blocks, const int* seq_lens, const int* cu_q,

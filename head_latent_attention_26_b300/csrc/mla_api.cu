@@ -36,6 +36,13 @@ bool tensor_path_dims(const mla_dims* d) {
   return d->n_h == 128 && d->d_c == 512 && d->d_hr == 64 && d->block == 64 && d->dtype == MLA_BF16;
 }
 
+// The projection kernels tile weights in 128-row slabs that must not straddle
+// heads, and stream k in 64-column (128-byte) steps.
+bool proj_tc_dims(const mla_dims* d) {
+  return d->dtype == MLA_BF16 && d->d_h == 128 && d->d_c % 128 == 0 && d->d_hr % 2 == 0 &&
+         d->d_model % 64 == 0 && d->d_cq % 64 == 0 && (d->d_c + d->d_hr) % 8 == 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -63,6 +70,7 @@ mla_status mla_create(const mla_dims* dims, int max_pos, mla_handle** out) {
   h->max_pos = max_pos;
   h->wait_limit = mla::kDefaultWaitLimit;
   h->tensor_path = tensor_path_dims(dims);
+  h->proj_tc = proj_tc_dims(dims);
   if (cudaGetDevice(&h->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
     delete h;
@@ -124,6 +132,14 @@ mla_status mla_q_proj(mla_handle* h, const void* x, const void* w_dq, const void
     if (!p || !aligned16(p)) return MLA_ERR_INVALID_ARG;
   if (!ws || !aligned16(ws) || ws_bytes < mla_q_proj_workspace_bytes(h, n_tok)) return MLA_ERR_WORKSPACE;
   const mla_dims& d = h->dims;
+  if (h->proj_tc) {
+    MLA_TRY_CUDA(mla::launch_linear_tc(h, x, d.d_model, w_dq, d.d_model, d.d_cq, 1, 0, ws, d.d_cq, n_tok, stream));
+    MLA_TRY_CUDA(mla::launch_linear_tc(h, ws, d.d_cq, w_uq, d.d_cq, d.n_h * d.d_h, 1, 0, q_c, d.n_h * d.d_h, n_tok,
+                                       stream));
+    MLA_TRY_CUDA(mla::launch_linear_tc(h, ws, d.d_cq, w_qr, d.d_cq, d.n_h * d.d_hr, 1, 0, q_r, d.n_h * d.d_hr,
+                                       n_tok, stream));
+    return MLA_OK;
+  }
   MLA_TRY_CUDA(mla::launch_linear(h, x, d.d_model, w_dq, d.d_model, d.d_cq, ws, d.d_cq, n_tok, stream));
   MLA_TRY_CUDA(mla::launch_linear(h, ws, d.d_cq, w_uq, d.d_cq, d.n_h * d.d_h, q_c, d.n_h * d.d_h, n_tok,
                                   stream));
@@ -143,6 +159,11 @@ mla_status mla_cache_append(mla_handle* h, const void* x, const void* w_dkr, con
   if (!seq_idx || !pos || !block_table || !aligned4(seq_idx) || !aligned4(pos) || !aligned4(block_table))
     return MLA_ERR_INVALID_ARG;
   if (max_blocks < 1 || batch < 1 || n_pool_blocks < 1) return MLA_ERR_INVALID_ARG;
+  if (h->proj_tc) {
+    MLA_TRY_CUDA(mla::launch_cache_append_tc(h, x, w_dkr, seq_idx, pos, n_new, block_table, max_blocks, batch,
+                                             pool, n_pool_blocks, stream));
+    return MLA_OK;
+  }
   MLA_TRY_CUDA(mla::launch_cache_append_simt(h, x, w_dkr, seq_idx, pos, n_new, block_table, max_blocks,
                                              batch, pool, n_pool_blocks, stream));
   return MLA_OK;
@@ -156,6 +177,10 @@ mla_status mla_absorb_q(mla_handle* h, const void* q_c, const void* q_r, const i
   for (const void* p : {q_c, q_r, w_uk, static_cast<const void*>(q_lat)})
     if (!p || !aligned16(p)) return MLA_ERR_INVALID_ARG;
   if (!pos || !aligned4(pos)) return MLA_ERR_INVALID_ARG;
+  if (h->proj_tc) {
+    MLA_TRY_CUDA(mla::launch_absorb_q_tc(h, q_c, q_r, pos, n_tok, w_uk, q_lat, stream));
+    return MLA_OK;
+  }
   MLA_TRY_CUDA(mla::launch_absorb_q_simt(h, q_c, q_r, pos, n_tok, w_uk, q_lat, stream));
   return MLA_OK;
 }
@@ -229,6 +254,11 @@ mla_status mla_out(mla_handle* h, const void* o_lat, const void* w_uv, const voi
   if (!ws || !aligned16(ws) || ws_bytes < mla_out_workspace_bytes(h, n_tok)) return MLA_ERR_WORKSPACE;
   const mla_dims& d = h->dims;
   const int H = d.n_h * d.d_h;
+  if (h->proj_tc) {
+    MLA_TRY_CUDA(mla::launch_linear_tc(h, o_lat, d.n_h * d.d_c, w_uv, d.d_c, H, d.n_h, d.d_c, ws, H, n_tok, stream));
+    MLA_TRY_CUDA(mla::launch_linear_tc(h, ws, H, w_o, H, d.d_model, 1, 0, u, d.d_model, n_tok, stream));
+    return MLA_OK;
+  }
   MLA_TRY_CUDA(mla::launch_up_project_simt(h, o_lat, w_uv, n_tok, ws, stream));
   MLA_TRY_CUDA(mla::launch_linear(h, ws, H, w_o, H, d.d_model, u, d.d_model, n_tok, stream));
   return MLA_OK;

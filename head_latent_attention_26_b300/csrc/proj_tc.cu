@@ -1,0 +1,464 @@
+// proj_tc.cu -- the projection steps of the layer on sm_103a tensor cores.
+//
+// Every projection of the decode step is a skinny product Y[n, o] =
+// sum_k X[n, k] W[o, k]: a few new tokens (n) against a weight matrix that is
+// read once per step.  The work is bound by streaming the weights out of HBM,
+// so the kernel is built around that stream:
+// * the weight rows are the M = 128 side of every tcgen05 MMA and the tokens
+//   the N side (N = 64, 128 or 256 per tile), accumulators in TMEM;
+// * one warp issues TMA loads of 128 x 64 weight tiles (128B swizzle, L2
+//   evict-first) and token tiles (evict-last: every output tile re-reads
+//   them) into a ring of shared-memory stages, one thread issues the MMAs;
+// * when one output tile has too few k-blocks to keep enough SMs streaming,
+//   the k range is split over the CTAs of a thread-block cluster and the fp32
+//   partial tiles are summed through distributed shared memory in a fixed
+//   order, so no global workspace or second kernel is needed.
+//
+// Three epilogues serve the steps of the path:
+// * linear: Y[n, o] in bf16 -- c^Q = W^DQ h, q^C = W^UQ c^Q, W^QR c^Q
+//   ([qiita] "Query の圧縮", "RoPE の扱い"), o_i = W^UV_i o~_i per head and
+//   u = W^O [o_1; ...] ([kasblo] "V側は、小さな表現の加重和を先に求める",
+//   [qiita] "Attention 計算");
+// * append: the cache row [c^KV ; RoPE_pos(k^R)] = [W^DKV h ; RoPE(W^KR h)]
+//   ([0h-n0] "MLA: 低ランクKV結合圧縮", [qiita] "RoPE の扱い") rounded once to
+//   bf16 and written to pool row block_table[b][pos/64]*64 + pos%64;
+// * absorb: q~_i = W^UK_i^T q^C_i ([0h-n0] "行列吸収トリック") with the W^UK
+//   tile read as an MN-major A operand (no transpose copy), plus the RoPE of
+//   q^R_i, written as one latent query row [q~_i ; RoPE_pos(q^R_i)].
+//
+// [0h-n0] = "論文解説: DeepSeek-V2 — … Multi-head Latent Attention",
+// [qiita] = MLA notes on qiita.com, [kasblo] = MLA explainer on kasblo.com.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kBM = 128;                       // weight rows per output tile
+constexpr int kBK = 64;                        // k per stage (one 128-byte swizzle atom)
+constexpr uint32_t kABytes = kBM * kBK * 2;    // 16 KB weight tile
+constexpr int kThreads = 128;
+constexpr int kMaxSplit = 8;                   // portable cluster size
+
+enum : int { kModeLinear = 0, kModeAppend = 1, kModeAbsorb = 2 };
+
+struct ProjMaps {
+  CUtensorMap w;  // weights
+  CUtensorMap x;  // tokens
+};
+
+struct ProjParams {
+  int n_tok, out, k_blocks;
+  int tiles_per_group;  // output tiles sharing one window of X columns
+  int x_group_cols;     // X column offset of group g = g * x_group_cols
+  int w_group_rows;     // absorb: W^UK row offset of head g = g * w_group_rows
+  __nv_bfloat16* y;
+  long long ldy;
+  // append
+  const int* seq_idx;
+  const int* pos;
+  const int* block_table;
+  int max_blocks, batch, n_pool_blocks, max_pos, d_c, d_hr, width, block;
+  __nv_bfloat16* pool;
+  const float* rope_cos;
+  const float* rope_sin;
+  // absorb
+  __nv_bfloat16* q_lat;
+  const __nv_bfloat16* q_r;
+  int n_h;
+  int* status;
+  long long wait_limit;
+};
+
+template <int STAGES, int NT>
+struct ProjShared {
+  uint64_t full[STAGES], empty[STAGES], done;
+  uint32_t tmem;
+  int abort;
+  int slot[NT];  // append: destination pool row of each token of the tile (-1 = skip)
+  int tpos[NT];  // append: its position
+};
+
+__device__ __forceinline__ bool proj_wait(uint64_t* bar, uint32_t parity, const ProjParams& p, int* abort) {
+  for (long long i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (i >= p.wait_limit || *reinterpret_cast<volatile int*>(abort)) {
+      report(p.status, MLA_ERR_DEVICE_TIMEOUT);
+      atomicExch(abort, 1);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void store_pair(__nv_bfloat16* dst, float a, float b) {
+  *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(a, b);
+}
+
+template <int NT, int STAGES, int MODE>
+__global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p) {
+  constexpr uint32_t kBBytes = NT * kBK * 2;
+  constexpr uint32_t kStage = kABytes + kBBytes;
+  constexpr uint32_t kRedCols = 64;  // epilogue chunk: 64 token columns of fp32
+  static_assert(STAGES * kStage >= kRedCols * kBM * 4, "reduction buffer reuses the stages");
+  using Shared = ProjShared<STAGES, NT>;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Shared* ss = reinterpret_cast<Shared*>(smem + STAGES * kStage);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = static_cast<int>(cluster_ctarank());
+  const int nsplit = static_cast<int>(cluster_nctarank());
+  const int o_tile = blockIdx.y, n0 = blockIdx.z * NT;
+  const int group = o_tile / p.tiles_per_group;
+  const int kb0 = static_cast<int>(static_cast<long long>(split) * p.k_blocks / nsplit);
+  const int kb1 = static_cast<int>(static_cast<long long>(split + 1) * p.k_blocks / nsplit);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ss->full[s], 1);
+      mbar_init(&ss->empty[s], 1);
+    }
+    mbar_init(&ss->done, 1);
+    ss->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ss->tmem, NT);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ss->tmem;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&maps.w);
+      tma_prefetch_desc(&maps.x);
+      const uint64_t pol_w = l2_policy_evict_first(), pol_x = l2_policy_evict_last();
+      const int x_off = group * p.x_group_cols;
+      uint32_t it = 0;
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        const int s = it % STAGES;
+        if (it >= STAGES && !proj_wait(&ss->empty[s], ((it / STAGES) - 1) & 1, p, &ss->abort)) break;
+        uint8_t* st = smem + s * kStage;
+        mbar_arrive_expect_tx(&ss->full[s], kStage);
+        if (MODE == kModeAbsorb) {
+          // W^UK_i^T tile: 64 rows of head i (the k side) x 128 latent columns (the M side)
+          const int m = o_tile % p.tiles_per_group;
+          const int y = group * p.w_group_rows + kb * kBK;
+          tma_load_2d_hint(st, &maps.w, &ss->full[s], m * kBM, y, pol_w);
+          tma_load_2d_hint(st + kABytes / 2, &maps.w, &ss->full[s], m * kBM + 64, y, pol_w);
+        } else {
+          tma_load_2d_hint(st, &maps.w, &ss->full[s], kb * kBK, o_tile * kBM, pol_w);
+        }
+        tma_load_2d_hint(st + kABytes, &maps.x, &ss->full[s], x_off + kb * kBK, n0, pol_x);
+      }
+      if (ss->abort) {
+        // every issued copy must land before the CTA may exit
+        for (uint32_t k = (it > STAGES ? it - STAGES : 0); k < it; ++k)
+          for (long long i = 0; i < p.wait_limit && !mbar_try_wait(&ss->full[k % STAGES], (k / STAGES) & 1); ++i) {
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kBM, NT, MODE == kModeAbsorb, false);
+      uint32_t it = 0;
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        const int s = it % STAGES;
+        if (!proj_wait(&ss->full[s], (it / STAGES) & 1, p, &ss->abort)) break;
+        tc_fence_after();
+        const uint32_t a = smem_u32(smem + s * kStage), b = a + kABytes;
+#pragma unroll
+        for (int ks = 0; ks < kBK / 16; ++ks) {
+          const uint64_t ad = MODE == kModeAbsorb ? smem_desc(a + ks * 2048, 8192, 1024, kSwizzle128B)
+                                                  : smem_desc(a + ks * 32, 16, 1024, kSwizzle128B);
+          const uint64_t bd = smem_desc(b + ks * 32, 16, 1024, kSwizzle128B);
+          mma_ss(tmem, ad, bd, idesc, (it > 0 || ks > 0) ? 1u : 0u);
+        }
+        mma_commit(&ss->empty[s]);
+      }
+      mma_commit(&ss->done);  // arrives once every MMA above has finished
+    }
+  } else if (MODE == kModeAppend) {
+    // ---------------------------------------------------------------- destination rows
+    for (int j = threadIdx.x - 64; j < NT; j += 64) {
+      const int n = n0 + j;
+      int slot = -1, tp = 0;
+      if (n < p.n_tok) {
+        const int b = __ldg(p.seq_idx + n);
+        tp = __ldg(p.pos + n);
+        if (b < 0 || b >= p.batch || tp < 0 || tp >= p.max_pos || tp / p.block >= p.max_blocks) {
+          report(p.status, MLA_ERR_DEVICE_BOUNDS);
+        } else {
+          const int blk = __ldg(p.block_table + static_cast<size_t>(b) * p.max_blocks + tp / p.block);
+          if (blk < 0 || blk >= p.n_pool_blocks) report(p.status, MLA_ERR_DEVICE_BOUNDS);
+          else slot = blk * p.block + tp % p.block;
+        }
+      }
+      ss->slot[j] = slot;
+      ss->tpos[j] = tp;
+    }
+  }
+  __syncthreads();
+
+  // -------------------------------------------------------------------- epilogue
+  bool ok = proj_wait(&ss->done, 0, p, &ss->abort) && !*reinterpret_cast<volatile int*>(&ss->abort);
+  tc_fence_after();
+  float* red = reinterpret_cast<float*>(smem);  // [64 columns][128 rows] fp32, stages reused
+  const uint32_t red_addr = smem_u32(red);
+  const int r = warp * 32 + lane;  // TMEM lane = output row of the tile
+  const int my_pairs = (kBM / 2 - split + nsplit - 1) / nsplit;  // row pairs p with p % nsplit == split
+  const int half = p.d_hr / 2;
+#pragma unroll 1
+  for (int c0 = 0; c0 < NT; c0 += kRedCols) {
+    if (ok) {
+#pragma unroll
+      for (int ch = 0; ch < kRedCols / 16; ++ch) {
+        uint32_t v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0 + ch * 16, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) red[(ch * 16 + j) * kBM + r] = __uint_as_float(v[j]);
+      }
+    }
+    if (nsplit > 1) {
+      cluster_arrive();
+      cluster_wait();
+    } else {
+      __syncthreads();
+    }
+    if (ok) {
+      for (int f = threadIdx.x; f < my_pairs * kRedCols; f += kThreads) {
+        const int col = f / my_pairs;
+        const int row = 2 * (split + (f % my_pairs) * nsplit);
+        const int n = n0 + c0 + col;
+        if (n >= p.n_tok) continue;
+        const uint32_t off = static_cast<uint32_t>((col * kBM + row) * 4);
+        float2 acc = make_float2(0.f, 0.f);
+        if (nsplit > 1) {
+          for (int q = 0; q < nsplit; ++q) {
+            const float2 v = ld_cluster_v2(map_to_rank(red_addr + off, q));
+            acc.x += v.x;
+            acc.y += v.y;
+          }
+        } else {
+          acc = *reinterpret_cast<const float2*>(reinterpret_cast<const uint8_t*>(red) + off);
+        }
+        if (MODE == kModeLinear) {
+          const int o = o_tile * kBM + row;
+          if (o < p.out) store_pair(p.y + static_cast<size_t>(n) * p.ldy + o, acc.x, acc.y);
+        } else if (MODE == kModeAppend) {
+          const int o = o_tile * kBM + row;
+          const int slot = ss->slot[c0 + col];
+          if (o >= p.out || slot < 0) continue;
+          __nv_bfloat16* dst = p.pool + static_cast<size_t>(slot) * p.width + o;
+          if (o < p.d_c) {
+            store_pair(dst, acc.x, acc.y);
+          } else {
+            const int k = (o - p.d_c) >> 1;
+            const size_t t = static_cast<size_t>(ss->tpos[c0 + col]) * half + k;
+            const float cs = __ldg(p.rope_cos + t), sn = __ldg(p.rope_sin + t);
+            store_pair(dst, acc.x * cs - acc.y * sn, acc.x * sn + acc.y * cs);
+          }
+        } else {
+          const int o = (o_tile % p.tiles_per_group) * kBM + row;  // latent column of head `group`
+          if (o < p.out)
+            store_pair(p.q_lat + (static_cast<size_t>(n) * p.n_h + group) * p.width + o, acc.x, acc.y);
+        }
+      }
+    }
+    if (nsplit > 1) {
+      cluster_arrive();  // the partial tiles stay until every CTA has read them
+      cluster_wait();
+    } else {
+      __syncthreads();
+    }
+  }
+  if (MODE == kModeAbsorb && ok && split == 0 && o_tile % p.tiles_per_group == 0) {
+    // the positional part of the latent query: RoPE_pos(q^R_i) ([qiita] "RoPE の扱い")
+    for (int f = threadIdx.x; f < NT * half; f += kThreads) {
+      const int n = n0 + f / half, k = f % half;
+      if (n >= p.n_tok) break;
+      const int tp = __ldg(p.pos + n);
+      if (tp < 0 || tp >= p.max_pos) {
+        report(p.status, MLA_ERR_DEVICE_BOUNDS);
+        continue;
+      }
+      const size_t hn = static_cast<size_t>(n) * p.n_h + group;
+      const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(p.q_r + hn * p.d_hr + 2 * k);
+      const float x0 = __bfloat162float(x.x), x1 = __bfloat162float(x.y);
+      const size_t t = static_cast<size_t>(tp) * half + k;
+      const float cs = __ldg(p.rope_cos + t), sn = __ldg(p.rope_sin + t);
+      store_pair(p.q_lat + hn * p.width + p.d_c + 2 * k, x0 * cs - x1 * sn, x0 * sn + x1 * cs);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, NT);
+  }
+}
+
+template <int NT, int STAGES, int MODE>
+cudaError_t launch_proj_nt(const ProjMaps& maps, const ProjParams& p, int nsplit, int o_tiles, int n_tiles,
+                           cudaStream_t s) {
+  constexpr size_t kSmem = STAGES * (kABytes + NT * kBK * 2) + sizeof(ProjShared<STAGES, NT>) + 1024;
+  auto kern = proj_kernel<NT, STAGES, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nsplit, o_tiles, n_tiles);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = nsplit;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, maps, p);
+}
+
+// Token-tile width: the smallest of 64/128/256 that holds every token, else
+// 256-token tiles.  Stages: enough for ~100-150 KB of loads in flight.
+template <int MODE>
+cudaError_t launch_proj(const ProjMaps& maps, const ProjParams& p, int nsplit, int o_tiles, cudaStream_t s) {
+  if (p.n_tok <= 64) return launch_proj_nt<64, 4, MODE>(maps, p, nsplit, o_tiles, 1, s);
+  if (p.n_tok <= 128) return launch_proj_nt<128, 4, MODE>(maps, p, nsplit, o_tiles, 1, s);
+  return launch_proj_nt<256, 3, MODE>(maps, p, nsplit, o_tiles, (p.n_tok + 255) / 256, s);
+}
+
+int token_tile(int n_tok) { return n_tok <= 64 ? 64 : n_tok <= 128 ? 128 : 256; }
+
+// k-range split so that about two CTAs per SM (one for wide token tiles) stream weights.
+int pick_split(const mla_handle* h, int o_tiles, int n_tok, int k_blocks) {
+  const int nt = token_tile(n_tok);
+  const long long base = static_cast<long long>(o_tiles) * ((n_tok + nt - 1) / nt);
+  const long long target = static_cast<long long>(h->num_sms) * (nt == 64 ? 2 : 1);
+  long long sp = (target + base / 2) / base;
+  if (sp < 1) sp = 1;
+  if (sp > kMaxSplit) sp = kMaxSplit;
+  if (sp > k_blocks) sp = k_blocks;
+  return static_cast<int>(sp);
+}
+
+}  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tma_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+bool encode_bf16_2d(CUtensorMap* m, const void* base, long long cols, long long rows, int box_cols, int box_rows) {
+  auto enc = tma_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+ProjParams base_params(const mla_handle* h, int n_tok) {
+  ProjParams p = {};
+  p.n_tok = n_tok;
+  p.tiles_per_group = 1 << 30;
+  p.status = h->status;
+  p.wait_limit = h->wait_limit;
+  p.max_pos = h->max_pos;
+  p.d_c = h->dims.d_c;
+  p.d_hr = h->dims.d_hr;
+  p.width = h->dims.d_c + h->dims.d_hr;
+  p.block = h->dims.block;
+  p.n_h = h->dims.n_h;
+  p.rope_cos = h->rope_cos;
+  p.rope_sin = h->rope_sin;
+  return p;
+}
+}  // namespace
+
+cudaError_t launch_linear_tc(const mla_handle* h, const void* X, int x_cols, const void* W, int in, int out,
+                             int groups, int x_group_cols, void* Y, long long ldy, int n_tok, cudaStream_t s) {
+  ProjMaps maps;
+  const int nt = token_tile(n_tok);
+  if (!encode_bf16_2d(&maps.w, W, in, out, kBK, kBM) || !encode_bf16_2d(&maps.x, X, x_cols, n_tok, kBK, nt))
+    return cudaErrorInvalidValue;
+  ProjParams p = base_params(h, n_tok);
+  const int o_tiles = (out + kBM - 1) / kBM;
+  p.out = out;
+  p.k_blocks = (in + kBK - 1) / kBK;
+  p.tiles_per_group = groups > 1 ? o_tiles / groups : 1 << 30;
+  p.x_group_cols = groups > 1 ? x_group_cols : 0;
+  p.y = static_cast<__nv_bfloat16*>(Y);
+  p.ldy = ldy;
+  return launch_proj<kModeLinear>(maps, p, pick_split(h, o_tiles, n_tok, p.k_blocks), o_tiles, s);
+}
+
+cudaError_t launch_cache_append_tc(const mla_handle* h, const void* x, const void* w_dkr, const int* seq_idx,
+                                   const int* pos, int n_new, const int* block_table, int max_blocks, int batch,
+                                   void* pool, int n_pool_blocks, cudaStream_t s) {
+  const mla_dims& d = h->dims;
+  const int width = d.d_c + d.d_hr;
+  ProjMaps maps;
+  if (!encode_bf16_2d(&maps.w, w_dkr, d.d_model, width, kBK, kBM) ||
+      !encode_bf16_2d(&maps.x, x, d.d_model, n_new, kBK, token_tile(n_new)))
+    return cudaErrorInvalidValue;
+  ProjParams p = base_params(h, n_new);
+  const int o_tiles = (width + kBM - 1) / kBM;
+  p.out = width;
+  p.k_blocks = (d.d_model + kBK - 1) / kBK;
+  p.seq_idx = seq_idx;
+  p.pos = pos;
+  p.block_table = block_table;
+  p.max_blocks = max_blocks;
+  p.batch = batch;
+  p.n_pool_blocks = n_pool_blocks;
+  p.pool = static_cast<__nv_bfloat16*>(pool);
+  return launch_proj<kModeAppend>(maps, p, pick_split(h, o_tiles, n_new, p.k_blocks), o_tiles, s);
+}
+
+cudaError_t launch_absorb_q_tc(const mla_handle* h, const void* q_c, const void* q_r, const int* pos, int n_tok,
+                               const void* w_uk, void* q_lat, cudaStream_t s) {
+  const mla_dims& d = h->dims;
+  ProjMaps maps;
+  // W^UK as [n_h*d_h rows, d_c columns]; boxes of 64 rows x 64 latent columns
+  if (!encode_bf16_2d(&maps.w, w_uk, d.d_c, static_cast<long long>(d.n_h) * d.d_h, 64, kBK) ||
+      !encode_bf16_2d(&maps.x, q_c, static_cast<long long>(d.n_h) * d.d_h, n_tok, kBK, token_tile(n_tok)))
+    return cudaErrorInvalidValue;
+  ProjParams p = base_params(h, n_tok);
+  const int per_head = (d.d_c + kBM - 1) / kBM;
+  p.out = d.d_c;
+  p.k_blocks = (d.d_h + kBK - 1) / kBK;
+  p.tiles_per_group = per_head;
+  p.x_group_cols = d.d_h;
+  p.w_group_rows = d.d_h;
+  p.pos = pos;
+  p.q_lat = static_cast<__nv_bfloat16*>(q_lat);
+  p.q_r = static_cast<const __nv_bfloat16*>(q_r);
+  return launch_proj<kModeAbsorb>(maps, p, 1, per_head * d.n_h, s);
+}
+
+}  // namespace mla

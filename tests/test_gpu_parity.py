@@ -360,3 +360,62 @@ def test_bounded_wait_times_out_cleanly(v2):
     finally:
         v2.set_wait_limit(0)
     v2.check()
+
+
+# ---------------------------------------------------------------------------
+# Projection kernels at every token-tile width (64 / 128 / 256 and several
+# 256-token tiles), against the oracle's own projections
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n_tok", [1, 5, 64, 100, 300])
+def test_v2_projections_token_tiles(v2, n_tok):
+    d = V2
+    seed = 1020 + n_tok
+    W = synth.weights(d, seed, device="cuda")
+    x = synth.hidden(n_tok, d, seed, device="cuda")
+    q_c, q_r = v2.q_proj(x, W["W_dq"], W["W_uq"], W["W_qr"])
+    o_lat = synth.normal((n_tok, d.n_h, d.d_c), seed, "o_lat", device="cuda")
+    u = v2.out(o_lat, W["W_uv"], W["W_o"])
+    v2.check()
+    Wn = _np_weights(W)
+    _, qc_ref, qr_ref = O.query_parts(to_np(x), Wn["W_dq"], Wn["W_uq"], Wn["W_qr"], d.n_h)
+    rng = np.random.default_rng(seed)
+    for n in sorted(set(rng.choice(n_tok, min(n_tok, 6), replace=False).tolist()) | {n_tok - 1}):
+        assert row_rel_err(to_np(q_c[n]), qc_ref[n]) < OUT_TOL, n
+        assert row_rel_err(to_np(q_r[n]), qr_ref[n]) < OUT_TOL, n
+        u_ref = O.output_projection(O.up_project(to_np(o_lat[n]), Wn["W_uv"]), Wn["W_o"])
+        assert row_rel_err(to_np(u[n]), u_ref) < OUT_TOL, n
+
+
+def test_v2_cache_append_many_tokens(v2):
+    """300 new rows of 3 sequences in one call (two 256-token tiles)."""
+    d = V2
+    seq_lens = [180, 64, 56]
+    table, n_blocks, _, _, _ = batch_meta(seq_lens, [1, 1, 1], d.block, 1030, spare_blocks=1)
+    W = synth.weights(d, 1030, device="cuda")
+    x = synth.hidden(sum(seq_lens), d, 1030, device="cuda")
+    seq_idx = torch.tensor(sum([[b] * n for b, n in enumerate(seq_lens)], []), dtype=torch.int32, device="cuda")
+    pos = torch.tensor(sum([list(range(n)) for n in seq_lens], []), dtype=torch.int32, device="cuda")
+    pool = torch.zeros(n_blocks, d.block, d.width, dtype=torch.bfloat16, device="cuda")
+    v2.cache_append(x, _w_dkr(W), seq_idx, pos, table, pool)
+    v2.check()
+    c, k_r = O.kv_latent(to_np(x), to_np(W["W_dkv"]), to_np(W["W_kr"]), to_np(pos), d.rope_base)
+    tab = table.cpu()
+    slots = [O.cache_slot(tab, int(b), int(p), d.block) for b, p in zip(seq_idx.tolist(), pos.tolist())]
+    assert row_rel_err(to_np(pool.view(-1, d.width)[slots]), np.concatenate([c, k_r], axis=1)) < OUT_TOL
+
+
+@pytest.mark.parametrize("n_tok", [1, 70, 260])
+def test_v2_absorb_q_token_tiles(v2, n_tok):
+    d = V2
+    seed = 1040 + n_tok
+    W = synth.weights(d, seed, device="cuda")
+    q_c = synth.normal((n_tok, d.n_h, d.d_h), seed, "q_c", device="cuda")
+    q_r = synth.normal((n_tok, d.n_h, d.d_hr), seed, "q_r", device="cuda")
+    pos = torch.randint(0, MAX_POS, (n_tok,), generator=torch.Generator().manual_seed(seed),
+                        dtype=torch.int32).cuda()
+    q_lat = v2.absorb_q(q_c, q_r, pos, W["W_uk"])
+    v2.check()
+    for n in sorted({0, n_tok // 2, n_tok - 1}):
+        ref = O.absorb_query(to_np(q_c[n]), O.rope(to_np(q_r[n]), int(pos[n]), d.rope_base), to_np(W["W_uk"]))
+        assert row_rel_err(to_np(q_lat[n]), ref) < OUT_TOL, n
