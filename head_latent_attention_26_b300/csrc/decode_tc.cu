@@ -15,13 +15,16 @@
 // * Scores: CTA c computes the partial score over its 288 columns,
 //   S_c = Q~[:, own] . C[:, own]^T  (M=128, N=64, K=288), with its half of the
 //   latent query (latent and RoPE parts) resident in TMEM as the A operand.
-// * Each row warp (32 heads) ships its 32 x 64 block of partial scores, scaled
-//   to log2 units and rounded to fp16, straight from registers into the same
-//   warp's inbox in the peer CTA with st.async (completion counted on the
-//   peer's mbarrier, no fence), one tile ahead of the tile it combines, so the
-//   exchange hides behind a tile of work.  Both CTAs add the two fp16
-//   partials in fp32 (the sum commutes, so both get bit-identical scores) and
-//   run the same online softmax: no softmax state is exchanged.
+// * Each row warp (32 heads, one TMEM lane quadrant) ships its 32 x 64 block
+//   of partial scores, scaled to log2 units and rounded to fp16, straight from
+//   registers into the same warp's inbox in the peer CTA with st.async
+//   (completion counted on the peer's mbarrier, no fence), one tile ahead of
+//   the tile it combines, so the exchange hides behind a tile of work.  Each
+//   CTA adds the peer's fp16 partial to its own fp32 partial and runs the
+//   online softmax on the result; no softmax state is exchanged.  (The two
+//   CTAs' scores differ by the fp16 rounding of one partial, a few 1e-4 in
+//   log2 units; each CTA normalises its half of O with its own sum, so each
+//   half is a consistent softmax average.)
 // * Values: CTA c accumulates O[:, own 256 latent columns] += P . C[:, own]
 //   (M=128, N=256, K=64) in TMEM, with P (bf16) in TMEM and the key tile read
 //   again from the same shared-memory stage as an MN-major B operand.  No K or
@@ -37,7 +40,8 @@
 //   log-sum-exp combine kernel merges.
 //
 // Warp roles per CTA (192 threads): warp 0 = TMA producer, warp 1 = MMA
-// issuer + TMEM owner, warps 2..5 = "row" warps, thread = head (TMEM lane).
+// issuer + TMEM owner (the whole warp runs the loop, one elected lane issues
+// each batch of MMAs), warps 2..5 = "row" warps, thread = head (TMEM lane).
 // Every wait is bounded; a wait that runs out records MLA_ERR_DEVICE_TIMEOUT,
 // raises a CTA-wide abort flag and the roles drain and exit.
 #include <cuda.h>
@@ -60,11 +64,13 @@ constexpr int kBlockRows = 64;
 constexpr int kWidth = 576;             // d_c + d_hr
 constexpr int kDc = 512;
 constexpr int kStages = 5;
+constexpr int kPrefetchTiles = 6;      // tiles pulled into L2 ahead of the stage loads
 constexpr uint32_t kBoxBytes = kTile * 128;                 // 64 keys x 64 cols bf16 (128B swizzle)
 constexpr uint32_t kRopeBoxBytes = kTile * 64;              // 64 keys x 32 cols bf16 (64B swizzle)
 constexpr uint32_t kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;  // 36864
+constexpr int kRowWarps = 4;
 constexpr uint32_t kXBlockBytes = 32 * kTile * 2;           // one warp's 32 heads x 64 keys fp16
-constexpr uint32_t kXSlotBytes = 4 * kXBlockBytes;          // all four row warps
+constexpr uint32_t kXSlotBytes = kRowWarps * kXBlockBytes;  // all row warps
 constexpr uint32_t kOffStages = 0;
 constexpr uint32_t kOffInbox = kOffStages + kStages * kStageBytes;
 constexpr uint32_t kOffBars = kOffInbox + 2 * kXSlotBytes;
@@ -72,7 +78,7 @@ constexpr uint32_t kSmemBytes = kOffBars + 512 + 1024;      // + alignment slack
 // TMEM columns (512 allocated): O half | Q~ latent half | Q~ RoPE half | P | S
 // (bf16 operands hold two elements per 32-bit column)
 constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemQR = 384, kTmemP = 416, kTmemS = 448;
-constexpr int kThreads = 192;
+constexpr int kThreads = 64 + 32 * kRowWarps;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -100,14 +106,14 @@ struct Params {
 struct Bars {
   uint64_t full[kStages], empty[kStages];
   uint64_t q_ready, s_full, s_free, p_ready, p_free;
-  uint64_t xin_full[2][4];    // peer warp w's partial scores landed in inbox slot
-  uint64_t inbox_free[2][4];  // peer warp w has consumed the slot this CTA writes into
+  uint64_t xin_full[2][kRowWarps];    // peer warp w's partial scores landed in inbox slot
+  uint64_t inbox_free[2][kRowWarps];  // peer warp w has consumed the slot this CTA writes into
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
-constexpr uint32_t kBarSlot = 4 * sizeof(uint64_t);  // stride of one slot in the [2][4] barrier arrays
+constexpr uint32_t kBarSlot = kRowWarps * sizeof(uint64_t);  // stride of one slot in the [2][8] barrier arrays
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Params& p, Bars* bs,
                                          bool cluster_scope = false) {
@@ -119,6 +125,14 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const P
       return false;
     }
   }
+}
+
+// The same for a warp that runs converged: lane 0 polls, every lane gets the
+// outcome (and elect.sync later picks lane 0, the lane that observed it).
+__device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, const Params& p, Bars* bs) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, p, bs);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
 // Contiguous slice [lo, hi) of the global tile list handled by worker g.
@@ -181,9 +195,6 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
-__device__ __forceinline__ float2 unpack_half2(uint32_t v) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&v));
-}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
@@ -200,13 +211,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&bs->full[s], 1);
       mbar_init(&bs->empty[s], 1);
     }
-    mbar_init(&bs->q_ready, 4);
+    mbar_init(&bs->q_ready, kRowWarps);
     mbar_init(&bs->s_full, 1);
-    mbar_init(&bs->s_free, 4);
-    mbar_init(&bs->p_ready, 4);
+    mbar_init(&bs->s_free, kRowWarps);
+    mbar_init(&bs->p_ready, kRowWarps);
     mbar_init(&bs->p_free, 1);
     for (int s = 0; s < 2; ++s)
-      for (int w = 0; w < 4; ++w) {
+      for (int w = 0; w < kRowWarps; ++w) {
         mbar_init(&bs->xin_full[s][w], 1);
         mbar_init(&bs->inbox_free[s][w], 1);
       }
@@ -215,7 +226,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     // first phase of every inbox barrier: one arrival (this one) + the bytes
     for (int s = 0; s < 2; ++s)
-      for (int w = 0; w < 4; ++w) mbar_arrive_expect_tx(&bs->xin_full[s][w], kXBlockBytes);
+      for (int w = 0; w < kRowWarps; ++w) mbar_arrive_expect_tx(&bs->xin_full[s][w], kXBlockBytes);
   }
   if (warp == 1) {
     tmem_alloc(&bs->tmem_base, 512);
@@ -233,6 +244,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&maps.latent);
       tma_prefetch_desc(&maps.rope);
       const uint64_t pol = l2_policy_evict_first();  // every cache row is read once
+      // Physical pool row of tile t of sequence b (a bad table entry is
+      // reported and replaced by block 0).
+      auto tile_row = [&](int b, int t) -> int {
+        int blk = t < p.max_blocks ? __ldg(p.block_table + static_cast<size_t>(b) * p.max_blocks + t) : -1;
+        if (blk < 0 || blk >= p.n_pool_blocks) {
+          report(p.status, MLA_ERR_DEVICE_BOUNDS);
+          blk = 0;
+        }
+        return blk * kBlockRows;
+      };
+      // A second cursor walks kPrefetchTiles ahead and pulls those tiles into
+      // L2, so the loads into the (few) shared-memory stages see L2 latency.
+      UnitIter pit = make_iter(p, g);
+      Unit pu;
+      bool pvalid = pit.next(p, g, pu);
+      int pt = pvalid ? pu.ta : 0;
+      auto prefetch_next = [&]() {
+        if (!pvalid) return;
+        const int y = tile_row(pu.b, pt);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tma_prefetch_l2_2d(&maps.latent, 256 * c + 64 * j, y);
+        tma_prefetch_l2_2d(&maps.rope, 512 + 32 * c, y);
+        if (++pt >= pu.tb) {
+          pvalid = pit.next(p, g, pu);
+          if (pvalid) pt = pu.ta;
+        }
+      };
+      for (int i = 0; i < kPrefetchTiles; ++i) prefetch_next();
       UnitIter iter = make_iter(p, g);
       Unit u;
       uint32_t it = 0;
@@ -242,18 +281,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int s = it % kStages;
           if (it >= kStages) ok = wait_bar(&bs->empty[s], ((it / kStages) - 1) & 1, p, bs);
           if (!ok) break;
-          int blk = t < p.max_blocks ? __ldg(p.block_table + static_cast<size_t>(u.b) * p.max_blocks + t) : -1;
-          if (blk < 0 || blk >= p.n_pool_blocks) {
-            report(p.status, MLA_ERR_DEVICE_BOUNDS);
-            blk = 0;
-          }
+          const int y = tile_row(u.b, t);
           uint8_t* st = smem + kOffStages + s * kStageBytes;
           mbar_arrive_expect_tx(&bs->full[s], kStageBytes);
-          const int y = blk * kBlockRows;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             tma_load_2d_hint(st + j * kBoxBytes, &maps.latent, &bs->full[s], 256 * c + 64 * j, y, pol);
           tma_load_2d_hint(st + 4 * kBoxBytes, &maps.rope, &bs->full[s], 512 + 32 * c, y, pol);
+          prefetch_next();
         }
       }
       // drain: every issued stage must land before the CTA may exit
@@ -265,7 +300,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop (operands stay warp-uniform); one elected
+    // lane issues each tcgen05 instruction.
+    {
       const uint32_t idesc_s = idesc_bf16_f32(128, kTile, false, false);
       const uint32_t idesc_o = idesc_bf16_f32(128, 256, false, true);
       UnitIter iter = make_iter(p, g);
@@ -277,26 +314,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // S(k) into the single S buffer once the row warps have read S(k-1) out of it
       auto issue_s = [&]() -> bool {
         const uint32_t k = n_sq;
-        if (!wait_bar(&bs->full[k % kStages], (k / kStages) & 1, p, bs)) return false;
-        if (k >= 1 && !wait_bar(&bs->s_free, (k - 1) & 1, p, bs)) return false;
+        if (!wait_bar_warp(&bs->full[k % kStages], (k / kStages) & 1, p, bs)) return false;
+        if (k >= 1 && !wait_bar_warp(&bs->s_free, (k - 1) & 1, p, bs)) return false;
         tc_fence_after();
         const uint32_t st = smem_u32(smem + kOffStages + (k % kStages) * kStageBytes);
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-          const uint64_t bd = smem_desc(st + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024, kSwizzle128B);
-          mma_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, idesc_s, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          const uint64_t bd = smem_desc(st + 4 * kBoxBytes + kk * 32, 16, 512, kSwizzle64B);
-          mma_ts(tmem + kTmemS, tmem + kTmemQR + kk * 8, bd, idesc_s, 1);
-        }
-        mma_commit(&bs->s_full);
+        mma_score_tile_elect(tmem + kTmemS, tmem + kTmemQ, tmem + kTmemQR, smem_desc(st, 16, 1024, kSwizzle128B),
+                             smem_desc(st + 4 * kBoxBytes, 16, 512, kSwizzle64B), idesc_s);
+        mma_commit_elect(&bs->s_full);
         ++n_sq;
         return true;
       };
       while (ok && iter.next(p, g, u)) {
-        ok = wait_bar(&bs->q_ready, n_units & 1, p, bs);
+        ok = wait_bar_warp(&bs->q_ready, n_units & 1, p, bs);
         ++n_units;
         if (!ok) break;
         tc_fence_after();
@@ -305,22 +334,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (n > 1 && !(ok = issue_s())) break;
         for (uint32_t t = 0; t < n && ok; ++t) {
           if (t + 2 < n && !(ok = issue_s())) break;  // waits until the row warps hold S(t+1)
-          if (!(ok = wait_bar(&bs->p_ready, n_o & 1, p, bs))) break;
+          if (!(ok = wait_bar_warp(&bs->p_ready, n_o & 1, p, bs))) break;
           tc_fence_after();
           const uint32_t st = smem_u32(smem + kOffStages + ((it0 + t) % kStages) * kStageBytes);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = smem_desc(st + ks * 2048, kBoxBytes, 1024, kSwizzle128B);
-            mma_ts(tmem + kTmemO, tmem + kTmemP + ks * 8, bd, idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
-          }
-          mma_commit(&bs->p_free);
-          mma_commit(&bs->empty[(it0 + t) % kStages]);
+          mma_value_tile_elect(tmem + kTmemO, tmem + kTmemP, smem_desc(st, kBoxBytes, 1024, kSwizzle128B), idesc_o,
+                               t > 0 ? 1u : 0u);
+          mma_commit_elect(&bs->p_free);
+          mma_commit_elect(&bs->empty[(it0 + t) % kStages]);
           ++n_o;
         }
       }
       if (!ok) {
         // every issued MMA must finish before TMEM is released
-        mma_commit(&bs->drain);
+        mma_commit_elect(&bs->drain);
         for (long long i = 0; i < p.wait_limit && !mbar_try_wait(&bs->drain, 0); ++i) {
         }
       }
@@ -332,22 +358,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int tr = threadIdx.x - 64;       // 0..127 among the row warps
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     // this warp's 4 KB block of inbox slot s sits at inbox0 + s * kXSlotBytes,
-    // at the same offset in the peer; row = lane, 16-byte chunks XOR-swizzled
+    // at the same offset in the peer; row = lane (128 B), 16-byte chunks XOR-swizzled
     const uint8_t* const inbox0 = smem + kOffInbox + q * kXBlockBytes;
     const uint32_t peer_row0 = map_to_rank(smem_u32(inbox0 + lane * 128), peer);
     const uint32_t peer_xin0 = map_to_rank(smem_u32(&bs->xin_full[0][q]), peer);
     const uint32_t peer_free0 = map_to_rank(smem_u32(&bs->inbox_free[0][q]), peer);
+    const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
     UnitIter iter = make_iter(p, g);
     Unit u;
     uint32_t n_s = 0;      // S tiles read out of TMEM (global)
-    uint32_t n_send = 0;   // partial blocks sent to the peer (= received from it)
-    uint32_t n_recv = 0;
+    uint32_t n_send = 0;   // partial blocks sent to the peer
+    uint32_t n_recv = 0;   // partial blocks received from it
     uint32_t n_p = 0;      // P tiles written (global) = tile index for the stage ring
     bool ok = true;
 
-    // Reads S out of TMEM, scales it to log2 units, rounds it to fp16 (kept in
-    // `own`) and stores it into the peer's inbox.
-    auto send = [&](uint32_t* own) -> bool {
+    // Reads S out of TMEM and scales it to log2 units (kept in `own`, fp32);
+    // stores its fp16 rounding into the peer's inbox.
+    auto send = [&](float2* own) -> bool {
       if (!wait_bar(&bs->s_full, n_s & 1, p, bs)) return false;
       ++n_s;
       tc_fence_after();
@@ -358,15 +385,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bs->s_free);
+      uint32_t h[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        own[j] = pack_half2(__uint_as_float(v[2 * j]) * p.scale_log2, __uint_as_float(v[2 * j + 1]) * p.scale_log2);
+      for (int j = 0; j < 32; ++j) {
+        own[j] = mul_f32x2(make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), scale2);
+        h[j] = pack_half2(own[j].x, own[j].y);
+      }
       const uint32_t slot = n_send & 1;
       if (n_send >= 2 && !wait_bar(&bs->inbox_free[slot][q], ((n_send >> 1) - 1) & 1, p, bs, true)) return false;
       const uint32_t dst = peer_row0 + slot * kXSlotBytes, bar = peer_xin0 + slot * kBarSlot;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch)
-        st_async_v4(dst + ((ch ^ (lane & 7)) * 16), make_uint4(own[4 * ch], own[4 * ch + 1], own[4 * ch + 2], own[4 * ch + 3]),
+        st_async_v4(dst + ((ch ^ (lane & 7)) * 16), make_uint4(h[4 * ch], h[4 * ch + 1], h[4 * ch + 2], h[4 * ch + 3]),
                     bar);
       ++n_send;
       return true;
@@ -400,14 +430,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bs->q_ready);
       }
       const int n = u.tb - u.ta;
-      uint32_t mine[32], nxt[32];
-      if (!(ok = send(mine))) break;
+      float2 cur[32], nxt[32];  // key pairs (2j, 2j+1) of the tile being combined / the next tile
+      if (!(ok = send(cur))) break;
       float m = -INFINITY, l = 0.f;
       for (int tt = 0; tt < n && ok; ++tt) {
         const int t = u.ta + tt;
         if (tt + 1 < n && !(ok = send(nxt))) break;
-        // ---- 1. the peer's partial scores of this tile: s = own + peer (log2 units)
-        float s[64];
+        // ---- 1. s = own + peer partial scores of this tile (log2 units)
         const uint32_t rslot = n_recv & 1;
         {
           if (!(ok = wait_bar(&bs->xin_full[rslot][q], (n_recv >> 1) & 1, p, bs, true))) break;
@@ -417,38 +446,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
             const uint4 w = *reinterpret_cast<const uint4*>(row + ((ch ^ (lane & 7)) * 16));
-            const uint32_t pw[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 a = unpack_half2(mine[4 * ch + e]), b = unpack_half2(pw[e]);
-              s[8 * ch + 2 * e] = a.x + b.x;
-              s[8 * ch + 2 * e + 1] = a.y + b.y;
-            }
+            cur[4 * ch] = add_f32_f16x2(cur[4 * ch], w.x);
+            cur[4 * ch + 1] = add_f32_f16x2(cur[4 * ch + 1], w.y);
+            cur[4 * ch + 2] = add_f32_f16x2(cur[4 * ch + 2], w.z);
+            cur[4 * ch + 3] = add_f32_f16x2(cur[4 * ch + 3], w.w);
           }
         }
         // ---- 2. online softmax in the log2 domain, causal mask on the last tile
         const int valid = min(kTile, u.pos - t * kTile + 1);  // keys of this tile the token sees
-        float mt = -INFINITY;
+        if (valid < kTile) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          s[j] = (j < valid) ? s[j] : -INFINITY;
-          mt = fmaxf(mt, s[j]);
+          for (int j = 0; j < 32; ++j) {
+            if (2 * j >= valid) cur[j].x = -INFINITY;
+            if (2 * j + 1 >= valid) cur[j].y = -INFINITY;
+          }
         }
+        // tile max: a tree of 3-input maxima over the 64 scores
+        auto sv = [&](int i) -> float { return (i & 1) ? cur[i >> 1].y : cur[i >> 1].x; };
+        float mx[22];
+#pragma unroll
+        for (int j = 0; j < 21; ++j) mx[j] = max3(sv(3 * j), sv(3 * j + 1), sv(3 * j + 2));
+        mx[21] = sv(63);
+        float my[8];
+#pragma unroll
+        for (int j = 0; j < 7; ++j) my[j] = max3(mx[3 * j], mx[3 * j + 1], mx[3 * j + 2]);
+        my[7] = mx[21];
+        const float mt = max3(max3(my[0], my[1], my[2]), max3(my[3], my[4], my[5]), fmaxf(my[6], my[7]));
         float m_use = m, f = 1.f;
         if (tt == 0) {
           m_use = mt;
         } else if (mt > m + kRescaleThreshold) {
           m_use = mt;
-          f = exp2f(m - mt);
+          f = ex2_approx(m - mt);
         }
+        const float2 neg_m = make_float2(-m_use, -m_use);
         uint32_t pk[32];
-        float rowsum = 0.f;
+        float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float e0 = exp2f(s[2 * j] - m_use), e1 = exp2f(s[2 * j + 1] - m_use);
-          rowsum += e0 + e1;
-          pk[j] = pack_bf16x2(e0, e1);
+          const float2 x = add_f32x2(cur[j], neg_m);
+          const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          rs[j & 3] = add_f32x2(rs[j & 3], e);
+          pk[j] = pack_bf16x2(e.x, e.y);
         }
+        const float2 rs2 = add_f32x2(add_f32x2(rs[0], rs[1]), add_f32x2(rs[2], rs[3]));
+        const float rowsum = rs2.x + rs2.y;
         l = (tt == 0) ? rowsum : l * f + rowsum;
         m = m_use;
         // ---- 3. the previous O MMA is done (P is free); rescale O if the max moved; write P
@@ -471,7 +513,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // rows past the token's position may hold anything: zero them for the O MMA
         if (valid < kTile) {
           uint8_t* st = smem + kOffStages + (n_p % kStages) * kStageBytes;
-          for (int idx = tr; idx < (kTile - valid) * 32; idx += 128) {
+          for (int idx = tr; idx < (kTile - valid) * 32; idx += 32 * kRowWarps) {
             const int row = valid + (idx >> 5), box = (idx >> 3) & 3, ch = idx & 7;
             *reinterpret_cast<uint4*>(st + box * kBoxBytes + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
           }
@@ -485,7 +527,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         ++n_p;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) mine[j] = nxt[j];
+        for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
       }
       if (!ok) break;
       // ---- epilogue: O / l for this head and this CTA's 256 latent columns

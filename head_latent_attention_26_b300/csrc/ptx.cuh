@@ -159,6 +159,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+// Pull a box of the tensor into L2 ahead of its load (no shared memory used).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -216,6 +223,101 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Warp-converged forms: every lane of the warp executes them (so operands stay
+// warp-uniform and need no per-instruction register moves) and one elected
+// lane issues the instruction.
+__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+// One 64-key score tile, issued by one elected lane of a converged warp:
+// S (+)= Q~[:, own 256 latent] . C^T (16 K-steps, A in TMEM, B a 128B-swizzled
+// K-major stage) + Q~[:, own 32 RoPE] . C_rope^T (2 K-steps, 64B swizzle).
+// Descriptors advance by constants inside the block, so the warp-uniform
+// bases are moved to the uniform datapath once per tile.
+__device__ __forceinline__ void mma_score_tile_elect(uint32_t d_tmem, uint32_t a_lat, uint32_t a_rope,
+                                                     uint64_t b_lat, uint64_t b_rope, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred e, f, t;\n\t.reg .b64 bd;\n\t.reg .b32 ad;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 f, 0, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "add.u32 ad, %1, 0;\n\tadd.s64 bd, %3, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, f;\n\t"
+      "add.u32 ad, %1, 8;\n\tadd.s64 bd, %3, 2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 16;\n\tadd.s64 bd, %3, 4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 24;\n\tadd.s64 bd, %3, 6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 32;\n\tadd.s64 bd, %3, 512;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 40;\n\tadd.s64 bd, %3, 514;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 48;\n\tadd.s64 bd, %3, 516;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 56;\n\tadd.s64 bd, %3, 518;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 64;\n\tadd.s64 bd, %3, 1024;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 72;\n\tadd.s64 bd, %3, 1026;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 80;\n\tadd.s64 bd, %3, 1028;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 88;\n\tadd.s64 bd, %3, 1030;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 96;\n\tadd.s64 bd, %3, 1536;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 104;\n\tadd.s64 bd, %3, 1538;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 112;\n\tadd.s64 bd, %3, 1540;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 120;\n\tadd.s64 bd, %3, 1542;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %2, 0;\n\tadd.s64 bd, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %2, 8;\n\tadd.s64 bd, %4, 2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "}"
+      ::"r"(d_tmem), "r"(a_lat), "r"(a_rope), "l"(b_lat), "l"(b_rope), "r"(idesc)
+      : "memory");
+}
+// O (+)= P . C[:, own 256 latent] over 64 keys (4 K-steps of 16), A = P in
+// TMEM, B = the same stage read MN-major.  `accumulate` = 0 starts O afresh.
+__device__ __forceinline__ void mma_value_tile_elect(uint32_t d_tmem, uint32_t a_p, uint64_t b_desc, uint32_t idesc,
+                                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, f, t;\n\t.reg .b64 bd;\n\t.reg .b32 ad;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 f, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "add.u32 ad, %1, 0;\n\tadd.s64 bd, %2, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %3, f;\n\t"
+      "add.u32 ad, %1, 8;\n\tadd.s64 bd, %2, 128;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %3, t;\n\t"
+      "add.u32 ad, %1, 16;\n\tadd.s64 bd, %2, 256;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %3, t;\n\t"
+      "add.u32 ad, %1, 24;\n\tadd.s64 bd, %2, 384;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %3, t;\n\t"
+      "}"
+      ::"r"(d_tmem), "r"(a_p), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -260,6 +362,38 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
+}
+
+// 2^x on the SFU, flushing subnormal results to zero (x <= 8 here).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Packed fp32 pairs (one instruction for two lanes of arithmetic).
+__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&r);
+}
+__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&r);
+}
+// (a.x + lo(h), a.y + hi(h)) with h two fp16 values, added in fp32.
+__device__ __forceinline__ float2 add_f32_f16x2(float2 a, uint32_t h) {
+  float x, y;
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tadd.rn.f32.f16 %0, lo, %3;\n\tadd.rn.f32.f16 %1, hi, %4;\n\t}"
+      : "=f"(x), "=f"(y)
+      : "r"(h), "f"(a.x), "f"(a.y));
+  return make_float2(x, y);
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
