@@ -16,10 +16,13 @@
 //   S_c = Q~[:, own] . C[:, own]^T  (M=128, N=64, K=288), with its half of the
 //   latent query (latent and RoPE parts) resident in TMEM as the A operand.
 // * Each row warp (32 heads, one TMEM lane quadrant) ships its 32 x 64 block
-//   of partial scores, scaled to log2 units and rounded to fp16, straight from
-//   registers into the same warp's inbox in the peer CTA with st.async
+//   of partial scores, scaled to log2 units and rounded to fp16, to the same
+//   warp's inbox in the peer CTA with one bulk shared-to-shared copy
 //   (completion counted on the peer's mbarrier, no fence), one tile ahead of
-//   the tile it combines, so the exchange hides behind a tile of work.  Each
+//   the tile it combines, so the exchange hides behind a tile of work.  The
+//   exchange is bound by the SM-to-SM network (about 16 bytes per clock per
+//   SM on this part; bulk copies beat 16-byte st.async stores by 1.6x), which
+//   is why only fp16 partials travel.  Each
 //   CTA adds the peer's fp16 partial to its own fp32 partial and runs the
 //   online softmax on the result; no softmax state is exchanged.  (The two
 //   CTAs' scores differ by the fp16 rounding of one partial, a few 1e-4 in
@@ -63,17 +66,20 @@ constexpr int kTile = 64;               // keys per tile = rows per cache block
 constexpr int kBlockRows = 64;
 constexpr int kWidth = 576;             // d_c + d_hr
 constexpr int kDc = 512;
-constexpr int kStages = 5;
+constexpr int kStages = 5;             // latent stages (32 KB each)
+constexpr int kRopeSlots = 3;          // RoPE boxes live only until their score MMA
 constexpr int kPrefetchTiles = 6;      // tiles pulled into L2 ahead of the stage loads
 constexpr uint32_t kBoxBytes = kTile * 128;                 // 64 keys x 64 cols bf16 (128B swizzle)
 constexpr uint32_t kRopeBoxBytes = kTile * 64;              // 64 keys x 32 cols bf16 (64B swizzle)
-constexpr uint32_t kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;  // 36864
+constexpr uint32_t kStageBytes = 4 * kBoxBytes;             // 32768: the latent columns of a tile
 constexpr int kRowWarps = 4;
 constexpr uint32_t kXBlockBytes = 32 * kTile * 2;           // one warp's 32 heads x 64 keys fp16
 constexpr uint32_t kXSlotBytes = kRowWarps * kXBlockBytes;  // all row warps
 constexpr uint32_t kOffStages = 0;
-constexpr uint32_t kOffInbox = kOffStages + kStages * kStageBytes;
-constexpr uint32_t kOffBars = kOffInbox + 2 * kXSlotBytes;
+constexpr uint32_t kOffRope = kOffStages + kStages * kStageBytes;
+constexpr uint32_t kOffInbox = kOffRope + kRopeSlots * kRopeBoxBytes;
+constexpr uint32_t kOffOutbox = kOffInbox + 2 * kXSlotBytes;  // one slot: a copy reads it long before reuse
+constexpr uint32_t kOffBars = kOffOutbox + kXSlotBytes;
 constexpr uint32_t kSmemBytes = kOffBars + 512 + 1024;      // + alignment slack
 // TMEM columns (512 allocated): O half | Q~ latent half | Q~ RoPE half | P | S
 // (bf16 operands hold two elements per 32-bit column)
@@ -104,7 +110,7 @@ struct Params {
 };
 
 struct Bars {
-  uint64_t full[kStages], empty[kStages];
+  uint64_t full[kStages], empty[kStages], rope_empty[kRopeSlots];
   uint64_t q_ready, s_full, s_free, p_ready, p_free;
   uint64_t xin_full[2][kRowWarps];    // peer warp w's partial scores landed in inbox slot
   uint64_t inbox_free[2][kRowWarps];  // peer warp w has consumed the slot this CTA writes into
@@ -211,6 +217,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&bs->full[s], 1);
       mbar_init(&bs->empty[s], 1);
     }
+    for (int s = 0; s < kRopeSlots; ++s) mbar_init(&bs->rope_empty[s], 1);
     mbar_init(&bs->q_ready, kRowWarps);
     mbar_init(&bs->s_full, 1);
     mbar_init(&bs->s_free, kRowWarps);
@@ -280,14 +287,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int t = u.ta; t < u.tb && ok; ++t, ++it) {
           const int s = it % kStages;
           if (it >= kStages) ok = wait_bar(&bs->empty[s], ((it / kStages) - 1) & 1, p, bs);
+          const int rs = it % kRopeSlots;
+          if (ok && it >= kRopeSlots) ok = wait_bar(&bs->rope_empty[rs], ((it / kRopeSlots) - 1) & 1, p, bs);
           if (!ok) break;
           const int y = tile_row(u.b, t);
           uint8_t* st = smem + kOffStages + s * kStageBytes;
-          mbar_arrive_expect_tx(&bs->full[s], kStageBytes);
+          mbar_arrive_expect_tx(&bs->full[s], kStageBytes + kRopeBoxBytes);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             tma_load_2d_hint(st + j * kBoxBytes, &maps.latent, &bs->full[s], 256 * c + 64 * j, y, pol);
-          tma_load_2d_hint(st + 4 * kBoxBytes, &maps.rope, &bs->full[s], 512 + 32 * c, y, pol);
+          tma_load_2d_hint(smem + kOffRope + rs * kRopeBoxBytes, &maps.rope, &bs->full[s], 512 + 32 * c, y, pol);
           prefetch_next();
         }
       }
@@ -318,9 +327,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (k >= 1 && !wait_bar_warp(&bs->s_free, (k - 1) & 1, p, bs)) return false;
         tc_fence_after();
         const uint32_t st = smem_u32(smem + kOffStages + (k % kStages) * kStageBytes);
-        mma_score_tile_elect(tmem + kTmemS, tmem + kTmemQ, tmem + kTmemQR, smem_desc(st, 16, 1024, kSwizzle128B),
-                             smem_desc(st + 4 * kBoxBytes, 16, 512, kSwizzle64B), idesc_s);
+        const uint32_t rope = smem_u32(smem + kOffRope + (k % kRopeSlots) * kRopeBoxBytes);
+        mma_score_tile_elect<kBoxBytes>(tmem + kTmemS, tmem + kTmemQ, tmem + kTmemQR, smem_desc(st, 16, 1024, kSwizzle128B),
+                                        smem_desc(rope, 16, 512, kSwizzle64B), idesc_s);
         mma_commit_elect(&bs->s_full);
+        mma_commit_elect(&bs->rope_empty[k % kRopeSlots]);
         ++n_sq;
         return true;
       };
@@ -337,8 +348,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!(ok = wait_bar_warp(&bs->p_ready, n_o & 1, p, bs))) break;
           tc_fence_after();
           const uint32_t st = smem_u32(smem + kOffStages + ((it0 + t) % kStages) * kStageBytes);
-          mma_value_tile_elect(tmem + kTmemO, tmem + kTmemP, smem_desc(st, kBoxBytes, 1024, kSwizzle128B), idesc_o,
-                               t > 0 ? 1u : 0u);
+          mma_value_tile_elect<kTile / 16>(tmem + kTmemO, tmem + kTmemP, smem_desc(st, kBoxBytes, 1024, kSwizzle128B),
+                                           idesc_o, t > 0 ? 1u : 0u);
           mma_commit_elect(&bs->p_free);
           mma_commit_elect(&bs->empty[(it0 + t) % kStages]);
           ++n_o;
@@ -360,7 +371,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // this warp's 4 KB block of inbox slot s sits at inbox0 + s * kXSlotBytes,
     // at the same offset in the peer; row = lane (128 B), 16-byte chunks XOR-swizzled
     const uint8_t* const inbox0 = smem + kOffInbox + q * kXBlockBytes;
-    const uint32_t peer_row0 = map_to_rank(smem_u32(inbox0 + lane * 128), peer);
+    uint8_t* const outbox = smem + kOffOutbox + q * kXBlockBytes;
+    const uint32_t peer_inbox0 = map_to_rank(smem_u32(inbox0), peer);
     const uint32_t peer_xin0 = map_to_rank(smem_u32(&bs->xin_full[0][q]), peer);
     const uint32_t peer_free0 = map_to_rank(smem_u32(&bs->inbox_free[0][q]), peer);
     const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
@@ -373,7 +385,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
 
     // Reads S out of TMEM and scales it to log2 units (kept in `own`, fp32);
-    // stores its fp16 rounding into the peer's inbox.
+    // ships its fp16 rounding to the peer's inbox with one bulk copy.
     auto send = [&](float2* own) -> bool {
       if (!wait_bar(&bs->s_full, n_s & 1, p, bs)) return false;
       ++n_s;
@@ -392,14 +404,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         h[j] = pack_half2(own[j].x, own[j].y);
       }
       const uint32_t slot = n_send & 1;
-      if (n_send >= 2 && !wait_bar(&bs->inbox_free[slot][q], ((n_send >> 1) - 1) & 1, p, bs, true)) return false;
-      const uint32_t dst = peer_row0 + slot * kXSlotBytes, bar = peer_xin0 + slot * kBarSlot;
+      if (lane == 0) bulk_wait_read<0>();  // the previous copy has read the outbox
+      __syncwarp();
+      uint8_t* row = outbox + lane * 128;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch)
-        st_async_v4(dst + ((ch ^ (lane & 7)) * 16), make_uint4(h[4 * ch], h[4 * ch + 1], h[4 * ch + 2], h[4 * ch + 3]),
-                    bar);
+        *reinterpret_cast<uint4*>(row + ((ch ^ (lane & 7)) * 16)) = make_uint4(h[4 * ch], h[4 * ch + 1], h[4 * ch + 2], h[4 * ch + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      bool good = true;
+      if (lane == 0) {
+        if (n_send >= 2) good = wait_bar(&bs->inbox_free[slot][q], ((n_send >> 1) - 1) & 1, p, bs, true);
+        if (good) {
+          bulk_copy_to_peer(peer_inbox0 + slot * kXSlotBytes, outbox, kXBlockBytes, peer_xin0 + slot * kBarSlot);
+          bulk_commit();
+        }
+      }
       ++n_send;
-      return true;
+      return __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
     };
 
     while (ok && iter.next(p, g, u)) {
@@ -567,8 +589,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
     }
-    // a remote store into the peer must not outlive the peer: wait until the
-    // peer has consumed everything this warp sent (its inbox_free arrivals)
+    // a copy into the peer must not outlive the peer: wait until the peer has
+    // consumed everything this warp sent (its inbox_free arrivals)
+    if (lane == 0) bulk_wait_all();
     for (uint32_t k = (n_send > 2 ? n_send - 2 : 0); ok && k < n_send; ++k)
       ok = wait_bar(&bs->inbox_free[k & 1][q], (k >> 1) & 1, p, bs, true);
   }

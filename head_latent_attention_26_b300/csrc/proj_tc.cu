@@ -170,24 +170,26 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop (warp-uniform operands); one elected lane
+    // issues each k block's four MMAs.
+    {
       const uint32_t idesc = idesc_bf16_f32(kBM, NT, MODE == kModeAbsorb, false);
       uint32_t it = 0;
       for (int kb = kb0; kb < kb1; ++kb, ++it) {
         const int s = it % STAGES;
-        if (!proj_wait(&ss->full[s], (it / STAGES) & 1, p, &ss->abort)) break;
+        bool ok = true;
+        if (lane == 0) ok = proj_wait(&ss->full[s], (it / STAGES) & 1, p, &ss->abort);
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
         tc_fence_after();
         const uint32_t a = smem_u32(smem + s * kStage), b = a + kABytes;
-#pragma unroll
-        for (int ks = 0; ks < kBK / 16; ++ks) {
-          const uint64_t ad = MODE == kModeAbsorb ? smem_desc(a + ks * 2048, 8192, 1024, kSwizzle128B)
-                                                  : smem_desc(a + ks * 32, 16, 1024, kSwizzle128B);
-          const uint64_t bd = smem_desc(b + ks * 32, 16, 1024, kSwizzle128B);
-          mma_ss(tmem, ad, bd, idesc, (it > 0 || ks > 0) ? 1u : 0u);
-        }
-        mma_commit(&ss->empty[s]);
+        const uint64_t bd = smem_desc(b, 16, 1024, kSwizzle128B);
+        if (MODE == kModeAbsorb)
+          mma_ss_kblock_elect<128, 2>(tmem, smem_desc(a, 8192, 1024, kSwizzle128B), bd, idesc, it > 0 ? 1u : 0u);
+        else
+          mma_ss_kblock_elect<2, 2>(tmem, smem_desc(a, 16, 1024, kSwizzle128B), bd, idesc, it > 0 ? 1u : 0u);
+        mma_commit_elect(&ss->empty[s]);
       }
-      mma_commit(&ss->done);  // arrives once every MMA above has finished
+      mma_commit_elect(&ss->done);  // arrives once every MMA above has finished
     }
   } else if (MODE == kModeAppend) {
     // ---------------------------------------------------------------- destination rows
@@ -246,10 +248,15 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         const uint32_t off = static_cast<uint32_t>((col * kBM + row) * 4);
         float2 acc = make_float2(0.f, 0.f);
         if (nsplit > 1) {
-          for (int q = 0; q < nsplit; ++q) {
-            const float2 v = ld_cluster_v2(map_to_rank(red_addr + off, q));
-            acc.x += v.x;
-            acc.y += v.y;
+          // all partials in flight at once, then summed in rank order
+          float2 v[kMaxSplit];
+#pragma unroll
+          for (int q = 0; q < kMaxSplit; ++q)
+            v[q] = q < nsplit ? ld_cluster_v2(map_to_rank(red_addr + off, q)) : make_float2(0.f, 0.f);
+#pragma unroll
+          for (int q = 0; q < kMaxSplit; ++q) {
+            acc.x += v[q].x;
+            acc.y += v[q].y;
           }
         } else {
           acc = *reinterpret_cast<const float2*>(reinterpret_cast<const uint8_t*>(red) + off);
@@ -284,21 +291,25 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
       __syncthreads();
     }
   }
-  if (MODE == kModeAbsorb && ok && split == 0 && o_tile % p.tiles_per_group == 0) {
-    // the positional part of the latent query: RoPE_pos(q^R_i) ([qiita] "RoPE の扱い")
-    for (int f = threadIdx.x; f < NT * half; f += kThreads) {
+  if (MODE == kModeAbsorb && ok && split == 0) {
+    // the positional part of the latent query: RoPE_pos(q^R_i) ([qiita] "RoPE の扱い"),
+    // shared out over the head's output tiles; every load of an item is
+    // independent of the others, so they all go out before any is used
+    const int m = o_tile % p.tiles_per_group, nm = p.tiles_per_group;
+    const int items = NT * half;
+    for (int f = threadIdx.x + kThreads * m; f < items; f += kThreads * nm) {
       const int n = n0 + f / half, k = f % half;
-      if (n >= p.n_tok) break;
+      if (n >= p.n_tok) continue;
       const int tp = __ldg(p.pos + n);
+      const size_t hn = static_cast<size_t>(n) * p.n_h + group;
+      const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(p.q_r + hn * p.d_hr + 2 * k);
       if (tp < 0 || tp >= p.max_pos) {
         report(p.status, MLA_ERR_DEVICE_BOUNDS);
         continue;
       }
-      const size_t hn = static_cast<size_t>(n) * p.n_h + group;
-      const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(p.q_r + hn * p.d_hr + 2 * k);
-      const float x0 = __bfloat162float(x.x), x1 = __bfloat162float(x.y);
       const size_t t = static_cast<size_t>(tp) * half + k;
       const float cs = __ldg(p.rope_cos + t), sn = __ldg(p.rope_sin + t);
+      const float x0 = __bfloat162float(x.x), x1 = __bfloat162float(x.y);
       store_pair(p.q_lat + hn * p.width + p.d_c + 2 * k, x0 * cs - x1 * sn, x0 * sn + x1 * cs);
     }
   }
@@ -347,11 +358,10 @@ int pick_split(const mla_handle* h, int o_tiles, int n_tok, int k_blocks) {
   const int nt = token_tile(n_tok);
   const long long base = static_cast<long long>(o_tiles) * ((n_tok + nt - 1) / nt);
   const long long target = static_cast<long long>(h->num_sms) * (nt == 64 ? 2 : 1);
-  long long sp = (target + base / 2) / base;
-  if (sp < 1) sp = 1;
-  if (sp > kMaxSplit) sp = kMaxSplit;
-  if (sp > k_blocks) sp = k_blocks;
-  return static_cast<int>(sp);
+  // the largest power of two that keeps the grid within about one wave
+  int sp = 1;
+  while (sp * 2 <= kMaxSplit && sp * 2 <= k_blocks && base * sp * 2 <= target + target / 8) sp *= 2;
+  return sp;
 }
 
 }  // namespace

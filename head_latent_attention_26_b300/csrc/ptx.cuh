@@ -248,76 +248,92 @@ __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
       : "memory");
 }
-// One 64-key score tile, issued by one elected lane of a converged warp:
+// One score tile, issued by one elected lane of a converged warp:
 // S (+)= Q~[:, own 256 latent] . C^T (16 K-steps, A in TMEM, B a 128B-swizzled
-// K-major stage) + Q~[:, own 32 RoPE] . C_rope^T (2 K-steps, 64B swizzle).
-// Descriptors advance by constants inside the block, so the warp-uniform
-// bases are moved to the uniform datapath once per tile.
+// K-major stage of four 64-column boxes BOX bytes apart) + Q~[:, own 32 RoPE]
+// . C_rope^T (2 K-steps, 64B swizzle).  Descriptors advance by constants
+// inside the block, so the warp-uniform bases reach the uniform datapath once
+// per tile.
+template <int BOX>
 __device__ __forceinline__ void mma_score_tile_elect(uint32_t d_tmem, uint32_t a_lat, uint32_t a_rope,
                                                      uint64_t b_lat, uint64_t b_rope, uint32_t idesc) {
+  constexpr int kB = BOX / 16;  // box stride in descriptor units
   asm volatile(
       "{\n\t.reg .pred e, f, t;\n\t.reg .b64 bd;\n\t.reg .b32 ad;\n\t"
       "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 f, 0, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "add.u32 ad, %1, 0;\n\tadd.s64 bd, %3, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, f;\n\t"
-      "add.u32 ad, %1, 8;\n\tadd.s64 bd, %3, 2;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
-      "add.u32 ad, %1, 16;\n\tadd.s64 bd, %3, 4;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
-      "add.u32 ad, %1, 24;\n\tadd.s64 bd, %3, 6;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
-      "add.u32 ad, %1, 32;\n\tadd.s64 bd, %3, 512;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
-      "add.u32 ad, %1, 40;\n\tadd.s64 bd, %3, 514;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
-      "add.u32 ad, %1, 48;\n\tadd.s64 bd, %3, 516;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
-      "add.u32 ad, %1, 56;\n\tadd.s64 bd, %3, 518;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
-      "add.u32 ad, %1, 64;\n\tadd.s64 bd, %3, 1024;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
-      "add.u32 ad, %1, 72;\n\tadd.s64 bd, %3, 1026;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
-      "add.u32 ad, %1, 80;\n\tadd.s64 bd, %3, 1028;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
-      "add.u32 ad, %1, 88;\n\tadd.s64 bd, %3, 1030;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
-      "add.u32 ad, %1, 96;\n\tadd.s64 bd, %3, 1536;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
-      "add.u32 ad, %1, 104;\n\tadd.s64 bd, %3, 1538;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
-      "add.u32 ad, %1, 112;\n\tadd.s64 bd, %3, 1540;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
-      "add.u32 ad, %1, 120;\n\tadd.s64 bd, %3, 1542;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
-      "add.u32 ad, %2, 0;\n\tadd.s64 bd, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
-      "add.u32 ad, %2, 8;\n\tadd.s64 bd, %4, 2;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
-      "}"
-      ::"r"(d_tmem), "r"(a_lat), "r"(a_rope), "l"(b_lat), "l"(b_rope), "r"(idesc)
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %3, %5, f;\n\t"
+      "add.u32 ad, %1, 8;\n\tadd.s64 bd, %3, 2;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 16;\n\tadd.s64 bd, %3, 4;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 24;\n\tadd.s64 bd, %3, 6;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 32;\n\tadd.s64 bd, %3, %6;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 40;\n\tadd.s64 bd, %3, %7;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 48;\n\tadd.s64 bd, %3, %8;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 56;\n\tadd.s64 bd, %3, %9;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 64;\n\tadd.s64 bd, %3, %10;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 72;\n\tadd.s64 bd, %3, %11;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 80;\n\tadd.s64 bd, %3, %12;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 88;\n\tadd.s64 bd, %3, %13;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 96;\n\tadd.s64 bd, %3, %14;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 104;\n\tadd.s64 bd, %3, %15;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 112;\n\tadd.s64 bd, %3, %16;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "add.u32 ad, %1, 120;\n\tadd.s64 bd, %3, %17;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %4, %5, t;\n\t"
+      "add.u32 ad, %2, 8;\n\tadd.s64 bd, %4, 2;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %5, t;\n\t"
+      "}" ::"r"(d_tmem),
+      "r"(a_lat), "r"(a_rope), "l"(b_lat), "l"(b_rope), "r"(idesc), "n"(kB), "n"(kB + 2), "n"(kB + 4), "n"(kB + 6),
+      "n"(2 * kB), "n"(2 * kB + 2), "n"(2 * kB + 4), "n"(2 * kB + 6), "n"(3 * kB), "n"(3 * kB + 2), "n"(3 * kB + 4),
+      "n"(3 * kB + 6)
       : "memory");
 }
-// O (+)= P . C[:, own 256 latent] over 64 keys (4 K-steps of 16), A = P in
-// TMEM, B = the same stage read MN-major.  `accumulate` = 0 starts O afresh.
+// O (+)= P . C[:, own 256 latent] over KSTEPS x 16 keys, A = P in TMEM, B =
+// the same stage read MN-major.  `accumulate` = 0 starts O afresh.
+template <int KSTEPS>
 __device__ __forceinline__ void mma_value_tile_elect(uint32_t d_tmem, uint32_t a_p, uint64_t b_desc, uint32_t idesc,
                                                      uint32_t accumulate) {
+  static_assert(KSTEPS == 2 || KSTEPS == 4, "value tile of 32 or 64 keys");
+  if (KSTEPS == 2) {
+    asm volatile(
+        "{\n\t.reg .pred e, f, t;\n\t.reg .b64 bd;\n\t.reg .b32 ad;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 f, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, f;\n\t"
+        "add.u32 ad, %1, 8;\n\tadd.s64 bd, %2, 128;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %3, t;\n\t"
+        "}" ::"r"(d_tmem),
+        "r"(a_p), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred e, f, t;\n\t.reg .b64 bd;\n\t.reg .b32 ad;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 f, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, f;\n\t"
+        "add.u32 ad, %1, 8;\n\tadd.s64 bd, %2, 128;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %3, t;\n\t"
+        "add.u32 ad, %1, 16;\n\tadd.s64 bd, %2, 256;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %3, t;\n\t"
+        "add.u32 ad, %1, 24;\n\tadd.s64 bd, %2, 384;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %3, t;\n\t"
+        "}" ::"r"(d_tmem),
+        "r"(a_p), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
+}
+// Four K-steps of 16 (one 64-wide k block) with A and B in shared memory,
+// issued by one elected lane of a converged warp; descriptors advance by
+// A_STEP / B_STEP (16-byte units) per step.  `accumulate` = 0 starts D afresh.
+template <int A_STEP, int B_STEP>
+__device__ __forceinline__ void mma_ss_kblock_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                    uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred e, f, t;\n\t.reg .b64 bd;\n\t.reg .b32 ad;\n\t"
+      "{\n\t.reg .pred e, f, t;\n\t.reg .b64 ad, bd;\n\t"
       "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 f, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "add.u32 ad, %1, 0;\n\tadd.s64 bd, %2, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %3, f;\n\t"
-      "add.u32 ad, %1, 8;\n\tadd.s64 bd, %2, 128;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %3, t;\n\t"
-      "add.u32 ad, %1, 16;\n\tadd.s64 bd, %2, 256;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %3, t;\n\t"
-      "add.u32 ad, %1, 24;\n\tadd.s64 bd, %2, 384;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ad], bd, %3, t;\n\t"
-      "}"
-      ::"r"(d_tmem), "r"(a_p), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, f;\n\t"
+      "add.s64 ad, %1, %5;\n\tadd.s64 bd, %2, %6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.s64 ad, %1, %7;\n\tadd.s64 bd, %2, %8;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.s64 ad, %1, %9;\n\tadd.s64 bd, %2, %10;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(A_STEP), "n"(B_STEP), "n"(2 * A_STEP),
+      "n"(2 * B_STEP), "n"(3 * A_STEP), "n"(3 * B_STEP)
       : "memory");
 }
-
 // Arrive once on `bar` when every tcgen05.mma this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
