@@ -52,59 +52,80 @@ def _dist():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    """SM clock and throttle-reason samples every 5 ms while the timed region
+    runs (NVML, the library nvidia-smi reads; nvidia-smi itself as fallback)."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+               "sw_power_cap": 0x4}
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.lines = []
+    def __init__(self, torch_device: int):
+        self.dev = torch_device
+        self.samples = []
+        self.smax = None
+        self.stop_flag = threading.Event()
         self.thread = None
+        self.source = None
+
+    def _handle(self, nv):
+        props = torch.cuda.get_device_properties(self.dev)
+        bus = getattr(props, "pci_bus_id", None)
+        if bus is not None:
+            dom = getattr(props, "pci_domain_id", 0)
+            devid = getattr(props, "pci_device_id", 0)
+            try:
+                return nv.nvmlDeviceGetHandleByPciBusId_v2(f"{dom:08x}:{bus:02x}:{devid:02x}.0".encode())
+            except Exception:  # noqa: BLE001
+                pass
+        return nv.nvmlDeviceGetHandleByIndex(self.dev)
 
     def start(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
-            return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+            import pynvml as nv
+            nv.nvmlInit()
+            h = self._handle(nv)
+            self.smax = float(nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM))
+            get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.source = "nvml"
+
+            def run():
+                while not self.stop_flag.is_set():
+                    try:
+                        self.samples.append((float(nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)), int(get_reasons(h))))
+                    except Exception:  # noqa: BLE001
+                        pass
+                    time.sleep(0.005)
+        except Exception:  # noqa: BLE001
+            self.source = "nvidia-smi"
+
+            def run():
+                q = "clocks.sm,clocks.max.sm,clocks_event_reasons.active"
+                while not self.stop_flag.is_set():
+                    try:
+                        out = subprocess.run(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={q}",
+                                              "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                                             timeout=5).stdout.strip().split(",")
+                        self.smax = float(out[1])
+                        self.samples.append((float(out[0]), int(out[2].strip(), 16)))
+                    except Exception:  # noqa: BLE001
+                        pass
+                    time.sleep(0.1)
+        self.thread = threading.Thread(target=run, daemon=True)
         self.thread.start()
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.thread.join(timeout=2)
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                smax = float(f[2])
-            except ValueError:
-                continue
-            for nm, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        sm.sort()
+        self.stop_flag.set()
+        if self.thread is not None:
+            self.thread.join(timeout=10)
+        sm = sorted(x for x, _ in self.samples)
+        reasons = set()
+        for _, bits in self.samples:
+            for name, bit in self.REASONS.items():
+                if bits & bit:
+                    reasons.add(name)
         med = sm[len(sm) // 2] if sm else None
-        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": med, "sm_max_mhz": self.smax, "reasons": sorted(reasons), "samples": len(sm),
+                "source": self.source}
 
 
 # ---------------------------------------------------------------------------
@@ -407,8 +428,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--batch", type=int, default=B_DEFAULT)
     ap.add_argument("--seq-len", type=int, default=T_DEFAULT)
