@@ -69,81 +69,80 @@ def _dist():
     return ws, rank
 
 
+_SAMPLER = r"""
+import ctypes, sys, time
+lib = ctypes.CDLL("libnvidia-ml.so.1")
+assert lib.nvmlInit_v2() == 0
+h = ctypes.c_void_p()
+bus = sys.argv[1]
+if not bus or lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+    assert lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(int(sys.argv[2])), ctypes.byref(h)) == 0
+c, r = ctypes.c_uint(), ctypes.c_ulonglong()
+get_r = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or lib.nvmlDeviceGetCurrentClocksThrottleReasons
+if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(c)) == 0:
+    print("max", c.value, flush=True)
+while True:
+    if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(c)) == 0 and get_r(h, ctypes.byref(r)) == 0:
+        print(c.value, r.value, flush=True)
+    time.sleep(0.005)
+"""
+
+
 class ClockSampler:
     """SM clock and throttle-reason samples every 5 ms while the timed region
-    runs (NVML, the library nvidia-smi reads; nvidia-smi itself as fallback)."""
+    runs, read through NVML (the library nvidia-smi uses) by a separate
+    process so the sampling does not compete with this process for the GIL."""
 
     REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
                "sw_power_cap": 0x4}
 
     def __init__(self, torch_device: int):
         self.dev = torch_device
-        self.samples = []
-        self.smax = None
-        self.stop_flag = threading.Event()
+        self.proc = None
+        self.lines = []
         self.thread = None
-        self.source = None
 
-    def _handle(self, nv):
+    def _bus_id(self) -> str:
         props = torch.cuda.get_device_properties(self.dev)
         bus = getattr(props, "pci_bus_id", None)
-        if bus is not None:
-            dom = getattr(props, "pci_domain_id", 0)
-            devid = getattr(props, "pci_device_id", 0)
-            try:
-                return nv.nvmlDeviceGetHandleByPciBusId_v2(f"{dom:08x}:{bus:02x}:{devid:02x}.0".encode())
-            except Exception:  # noqa: BLE001
-                pass
-        return nv.nvmlDeviceGetHandleByIndex(self.dev)
+        if bus is None:
+            return ""
+        return f"{getattr(props, 'pci_domain_id', 0):08x}:{bus:02x}:{getattr(props, 'pci_device_id', 0):02x}.0"
 
     def start(self):
         try:
-            import pynvml as nv
-            nv.nvmlInit()
-            h = self._handle(nv)
-            self.smax = float(nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM))
-            get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                nv.nvmlDeviceGetCurrentClocksThrottleReasons
-            self.source = "nvml"
-
-            def run():
-                while not self.stop_flag.is_set():
-                    try:
-                        self.samples.append((float(nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)), int(get_reasons(h))))
-                    except Exception:  # noqa: BLE001
-                        pass
-                    time.sleep(0.005)
-        except Exception as e:  # noqa: BLE001
-            self.source = f"nvidia-smi (nvml: {type(e).__name__}: {str(e)[:60]})"
-
-            def run():
-                q = "clocks.sm,clocks.max.sm,clocks_event_reasons.active"
-                while not self.stop_flag.is_set():
-                    try:
-                        out = subprocess.run(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={q}",
-                                              "--format=csv,noheader,nounits"], capture_output=True, text=True,
-                                             timeout=5).stdout.strip().split(",")
-                        self.smax = float(out[1])
-                        self.samples.append((float(out[0]), int(out[2].strip(), 16)))
-                    except Exception:  # noqa: BLE001
-                        pass
-                    time.sleep(0.1)
-        self.thread = threading.Thread(target=run, daemon=True)
+            self.proc = subprocess.Popen([sys.executable, "-c", _SAMPLER, self._bus_id(), str(self.dev)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=lambda: self.lines.extend(ln.strip() for ln in self.proc.stdout),
+                                       daemon=True)
         self.thread.start()
+        time.sleep(0.3)  # the sampler is up before the timed region starts
 
     def stop(self):
-        self.stop_flag.set()
-        if self.thread is not None:
-            self.thread.join(timeout=10)
-        sm = sorted(x for x, _ in self.samples)
-        reasons = set()
-        for _, bits in self.samples:
-            for name, bit in self.REASONS.items():
-                if bits & bit:
-                    reasons.add(name)
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["sampler unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        smax, sm, reasons = None, [], set()
+        for ln in self.lines:
+            f = ln.split()
+            if len(f) == 2 and f[0] == "max":
+                smax = float(f[1])
+            elif len(f) == 2:
+                sm.append(float(f[0]))
+                for name, bit in self.REASONS.items():
+                    if int(f[1]) & bit:
+                        reasons.add(name)
+        sm.sort()
         med = sm[len(sm) // 2] if sm else None
-        return {"sm_mhz": med, "sm_max_mhz": self.smax, "reasons": sorted(reasons), "samples": len(sm),
-                "source": self.source}
+        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm), "source": "nvml"}
 
 
 # ---------------------------------------------------------------------------
@@ -446,7 +445,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--batch", type=int, default=B_DEFAULT)

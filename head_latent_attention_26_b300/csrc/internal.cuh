@@ -92,6 +92,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tma_encoder();
 // tcgen05 projections (bf16, d_h = 128, widths multiples of 64)
 cudaError_t launch_linear_tc(const mla_handle* h, const void* X, int x_cols, const void* W, int in, int out,
                              int groups, int x_group_cols, void* Y, long long ldy, int n_tok, cudaStream_t s);
+// Two products of the same tokens in one launch: Y1 = X W1^T, Y2 = X W2^T.
+cudaError_t launch_linear2_tc(const mla_handle* h, const void* X, int in, const void* W1, int out1, void* Y1,
+                              long long ldy1, const void* W2, int out2, void* Y2, long long ldy2, int n_tok,
+                              cudaStream_t s);
 cudaError_t launch_cache_append_tc(const mla_handle* h, const void* x, const void* w_dkr, const int* seq_idx,
                                    const int* pos, int n_new, const int* block_table, int max_blocks, int batch,
                                    void* pool, int n_pool_blocks, cudaStream_t s);

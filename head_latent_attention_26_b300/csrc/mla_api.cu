@@ -134,10 +134,8 @@ mla_status mla_q_proj(mla_handle* h, const void* x, const void* w_dq, const void
   const mla_dims& d = h->dims;
   if (h->proj_tc) {
     MLA_TRY_CUDA(mla::launch_linear_tc(h, x, d.d_model, w_dq, d.d_model, d.d_cq, 1, 0, ws, d.d_cq, n_tok, stream));
-    MLA_TRY_CUDA(mla::launch_linear_tc(h, ws, d.d_cq, w_uq, d.d_cq, d.n_h * d.d_h, 1, 0, q_c, d.n_h * d.d_h, n_tok,
-                                       stream));
-    MLA_TRY_CUDA(mla::launch_linear_tc(h, ws, d.d_cq, w_qr, d.d_cq, d.n_h * d.d_hr, 1, 0, q_r, d.n_h * d.d_hr,
-                                       n_tok, stream));
+    MLA_TRY_CUDA(mla::launch_linear2_tc(h, ws, d.d_cq, w_uq, d.n_h * d.d_h, q_c, d.n_h * d.d_h, w_qr,
+                                        d.n_h * d.d_hr, q_r, d.n_h * d.d_hr, n_tok, stream));
     return MLA_OK;
   }
   MLA_TRY_CUDA(mla::launch_linear(h, x, d.d_model, w_dq, d.d_model, d.d_cq, ws, d.d_cq, n_tok, stream));

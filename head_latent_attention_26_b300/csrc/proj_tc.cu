@@ -45,13 +45,14 @@ constexpr int kBM = 128;                       // weight rows per output tile
 constexpr int kBK = 64;                        // k per stage (one 128-byte swizzle atom)
 constexpr uint32_t kABytes = kBM * kBK * 2;    // 16 KB weight tile
 constexpr int kThreads = 128;
-constexpr int kMaxSplit = 8;                   // portable cluster size
+constexpr int kMaxSplit = 16;                  // cluster size (above 8 needs the non-portable opt-in)
 
 enum : int { kModeLinear = 0, kModeAppend = 1, kModeAbsorb = 2 };
 
 struct ProjMaps {
-  CUtensorMap w;  // weights
-  CUtensorMap x;  // tokens
+  CUtensorMap w;   // weights
+  CUtensorMap x;   // tokens
+  CUtensorMap w2;  // linear mode: weights of a second product with the same tokens
 };
 
 struct ProjParams {
@@ -61,6 +62,11 @@ struct ProjParams {
   int w_group_rows;     // absorb: W^UK row offset of head g = g * w_group_rows
   __nv_bfloat16* y;
   long long ldy;
+  // linear mode: output tiles >= seg1_tiles belong to a second product
+  // (maps.w2 -> y2) over the same tokens and k range
+  int seg1_tiles, out2;
+  __nv_bfloat16* y2;
+  long long ldy2;
   // append
   const int* seq_idx;
   const int* pos;
@@ -101,7 +107,9 @@ __device__ __forceinline__ void store_pair(__nv_bfloat16* dst, float a, float b)
   *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(a, b);
 }
 
-template <int NT, int STAGES, int MODE>
+// One CTA computes MT output tiles of 128 weight rows (one TMEM accumulator of
+// NT columns each) over its share [kb0, kb1) of the k blocks.
+template <int NT, int STAGES, int MODE, int MT>
 __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p) {
   constexpr uint32_t kBBytes = NT * kBK * 2;
   constexpr uint32_t kStage = kABytes + kBBytes;
@@ -115,8 +123,13 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = static_cast<int>(cluster_ctarank());
   const int nsplit = static_cast<int>(cluster_nctarank());
-  const int o_tile = blockIdx.y, n0 = blockIdx.z * NT;
-  const int group = o_tile / p.tiles_per_group;
+  const int n0 = blockIdx.z * NT;
+  // first output tile of this CTA; in linear mode tiles past seg1_tiles are
+  // tiles of the second product
+  const bool seg2 = MODE == kModeLinear && static_cast<int>(blockIdx.y) * MT >= p.seg1_tiles;
+  const int tile0 = static_cast<int>(blockIdx.y) * MT - (seg2 ? p.seg1_tiles : 0);
+  const CUtensorMap* wmap = seg2 ? &maps.w2 : &maps.w;
+  const int group = tile0 / p.tiles_per_group;  // all MT tiles share it (MT divides tiles_per_group)
   const int kb0 = static_cast<int>(static_cast<long long>(split) * p.k_blocks / nsplit);
   const int kb1 = static_cast<int>(static_cast<long long>(split + 1) * p.k_blocks / nsplit);
 
@@ -130,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&ss->tmem, NT);
+    tmem_alloc(&ss->tmem, NT * MT);
     tmem_relinquish();
   }
   __syncthreads();
@@ -140,26 +153,33 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&maps.w);
+      tma_prefetch_desc(wmap);
       tma_prefetch_desc(&maps.x);
       const uint64_t pol_w = l2_policy_evict_first(), pol_x = l2_policy_evict_last();
       const int x_off = group * p.x_group_cols;
       uint32_t it = 0;
-      for (int kb = kb0; kb < kb1; ++kb, ++it) {
-        const int s = it % STAGES;
-        if (it >= STAGES && !proj_wait(&ss->empty[s], ((it / STAGES) - 1) & 1, p, &ss->abort)) break;
-        uint8_t* st = smem + s * kStage;
-        mbar_arrive_expect_tx(&ss->full[s], kStage);
-        if (MODE == kModeAbsorb) {
-          // W^UK_i^T tile: 64 rows of head i (the k side) x 128 latent columns (the M side)
-          const int m = o_tile % p.tiles_per_group;
-          const int y = group * p.w_group_rows + kb * kBK;
-          tma_load_2d_hint(st, &maps.w, &ss->full[s], m * kBM, y, pol_w);
-          tma_load_2d_hint(st + kABytes / 2, &maps.w, &ss->full[s], m * kBM + 64, y, pol_w);
-        } else {
-          tma_load_2d_hint(st, &maps.w, &ss->full[s], kb * kBK, o_tile * kBM, pol_w);
+      bool go = true;
+      for (int mi = 0; mi < MT && go; ++mi) {
+        const int o_tile = tile0 + mi;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (it >= STAGES && !proj_wait(&ss->empty[s], ((it / STAGES) - 1) & 1, p, &ss->abort)) {
+            go = false;
+            break;
+          }
+          uint8_t* st = smem + s * kStage;
+          mbar_arrive_expect_tx(&ss->full[s], kStage);
+          if (MODE == kModeAbsorb) {
+            // W^UK_i^T tile: 64 rows of head i (the k side) x 128 latent columns (the M side)
+            const int m = o_tile % p.tiles_per_group;
+            const int y = group * p.w_group_rows + kb * kBK;
+            tma_load_2d_hint(st, wmap, &ss->full[s], m * kBM, y, pol_w);
+            tma_load_2d_hint(st + kABytes / 2, wmap, &ss->full[s], m * kBM + 64, y, pol_w);
+          } else {
+            tma_load_2d_hint(st, wmap, &ss->full[s], kb * kBK, o_tile * kBM, pol_w);
+          }
+          tma_load_2d_hint(st + kABytes, &maps.x, &ss->full[s], x_off + kb * kBK, n0, pol_x);
         }
-        tma_load_2d_hint(st + kABytes, &maps.x, &ss->full[s], x_off + kb * kBK, n0, pol_x);
       }
       if (ss->abort) {
         // every issued copy must land before the CTA may exit
@@ -175,19 +195,26 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     {
       const uint32_t idesc = idesc_bf16_f32(kBM, NT, MODE == kModeAbsorb, false);
       uint32_t it = 0;
-      for (int kb = kb0; kb < kb1; ++kb, ++it) {
-        const int s = it % STAGES;
-        bool ok = true;
-        if (lane == 0) ok = proj_wait(&ss->full[s], (it / STAGES) & 1, p, &ss->abort);
-        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-        tc_fence_after();
-        const uint32_t a = smem_u32(smem + s * kStage), b = a + kABytes;
-        const uint64_t bd = smem_desc(b, 16, 1024, kSwizzle128B);
-        if (MODE == kModeAbsorb)
-          mma_ss_kblock_elect<128, 2>(tmem, smem_desc(a, 8192, 1024, kSwizzle128B), bd, idesc, it > 0 ? 1u : 0u);
-        else
-          mma_ss_kblock_elect<2, 2>(tmem, smem_desc(a, 16, 1024, kSwizzle128B), bd, idesc, it > 0 ? 1u : 0u);
-        mma_commit_elect(&ss->empty[s]);
+      bool go = true;
+      for (int mi = 0; mi < MT && go; ++mi) {
+        const uint32_t d = tmem + mi * NT;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % STAGES;
+          bool ok = true;
+          if (lane == 0) ok = proj_wait(&ss->full[s], (it / STAGES) & 1, p, &ss->abort);
+          if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+            go = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = smem_u32(smem + s * kStage), b = a + kABytes;
+          const uint64_t bd = smem_desc(b, 16, 1024, kSwizzle128B);
+          if (MODE == kModeAbsorb)
+            mma_ss_kblock_elect<128, 2>(d, smem_desc(a, 8192, 1024, kSwizzle128B), bd, idesc, kb > kb0 ? 1u : 0u);
+          else
+            mma_ss_kblock_elect<2, 2>(d, smem_desc(a, 16, 1024, kSwizzle128B), bd, idesc, kb > kb0 ? 1u : 0u);
+          mma_commit_elect(&ss->empty[s]);
+        }
       }
       mma_commit_elect(&ss->done);  // arrives once every MMA above has finished
     }
@@ -219,15 +246,19 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
   float* red = reinterpret_cast<float*>(smem);  // [64 columns][128 rows] fp32, stages reused
   const uint32_t red_addr = smem_u32(red);
   const int r = warp * 32 + lane;  // TMEM lane = output row of the tile
-  const int my_pairs = (kBM / 2 - split + nsplit - 1) / nsplit;  // row pairs p with p % nsplit == split
+  // CTA `split` of the cluster finishes the 4-row groups [g0, g1) of each
+  // column: contiguous 16-byte reads, so the SM-to-SM transfers are whole
+  const int g0 = split * (kBM / 4) / nsplit, g1 = (split + 1) * (kBM / 4) / nsplit, my_groups = g1 - g0;
   const int half = p.d_hr / 2;
 #pragma unroll 1
-  for (int c0 = 0; c0 < NT; c0 += kRedCols) {
+  for (int cc = 0; cc < MT * NT; cc += kRedCols) {
+    const int mi = cc / NT, c0 = cc % NT;
+    const int o_tile = tile0 + mi;
     if (ok) {
 #pragma unroll
       for (int ch = 0; ch < kRedCols / 16; ++ch) {
         uint32_t v[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0 + ch * 16, v);
+        tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + cc + ch * 16, v);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) red[(ch * 16 + j) * kBM + r] = __uint_as_float(v[j]);
@@ -240,47 +271,56 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
       __syncthreads();
     }
     if (ok) {
-      for (int f = threadIdx.x; f < my_pairs * kRedCols; f += kThreads) {
-        const int col = f / my_pairs;
-        const int row = 2 * (split + (f % my_pairs) * nsplit);
+      for (int f = threadIdx.x; f < my_groups * kRedCols; f += kThreads) {
+        const int col = f / my_groups;
+        const int row0 = 4 * (g0 + f % my_groups);
         const int n = n0 + c0 + col;
         if (n >= p.n_tok) continue;
-        const uint32_t off = static_cast<uint32_t>((col * kBM + row) * 4);
-        float2 acc = make_float2(0.f, 0.f);
+        const uint32_t off = static_cast<uint32_t>((col * kBM + row0) * 4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (nsplit > 1) {
           // all partials in flight at once, then summed in rank order
-          float2 v[kMaxSplit];
+          float4 v[kMaxSplit];
 #pragma unroll
           for (int q = 0; q < kMaxSplit; ++q)
-            v[q] = q < nsplit ? ld_cluster_v2(map_to_rank(red_addr + off, q)) : make_float2(0.f, 0.f);
+            v[q] = q < nsplit ? ld_cluster_v4(map_to_rank(red_addr + off, q)) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int q = 0; q < kMaxSplit; ++q) {
             acc.x += v[q].x;
             acc.y += v[q].y;
+            acc.z += v[q].z;
+            acc.w += v[q].w;
           }
         } else {
-          acc = *reinterpret_cast<const float2*>(reinterpret_cast<const uint8_t*>(red) + off);
+          acc = *reinterpret_cast<const float4*>(reinterpret_cast<const uint8_t*>(red) + off);
         }
-        if (MODE == kModeLinear) {
-          const int o = o_tile * kBM + row;
-          if (o < p.out) store_pair(p.y + static_cast<size_t>(n) * p.ldy + o, acc.x, acc.y);
-        } else if (MODE == kModeAppend) {
-          const int o = o_tile * kBM + row;
-          const int slot = ss->slot[c0 + col];
-          if (o >= p.out || slot < 0) continue;
-          __nv_bfloat16* dst = p.pool + static_cast<size_t>(slot) * p.width + o;
-          if (o < p.d_c) {
-            store_pair(dst, acc.x, acc.y);
+        const float2 pr[2] = {make_float2(acc.x, acc.y), make_float2(acc.z, acc.w)};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int row = row0 + 2 * e;
+          const float2 a = pr[e];
+          if (MODE == kModeLinear) {
+            const int o = o_tile * kBM + row;
+            if (!seg2 && o < p.out) store_pair(p.y + static_cast<size_t>(n) * p.ldy + o, a.x, a.y);
+            if (seg2 && o < p.out2) store_pair(p.y2 + static_cast<size_t>(n) * p.ldy2 + o, a.x, a.y);
+          } else if (MODE == kModeAppend) {
+            const int o = o_tile * kBM + row;
+            const int slot = ss->slot[c0 + col];
+            if (o >= p.out || slot < 0) continue;
+            __nv_bfloat16* dst = p.pool + static_cast<size_t>(slot) * p.width + o;
+            if (o < p.d_c) {
+              store_pair(dst, a.x, a.y);
+            } else {
+              const int k = (o - p.d_c) >> 1;
+              const size_t t = static_cast<size_t>(ss->tpos[c0 + col]) * half + k;
+              const float cs = __ldg(p.rope_cos + t), sn = __ldg(p.rope_sin + t);
+              store_pair(dst, a.x * cs - a.y * sn, a.x * sn + a.y * cs);
+            }
           } else {
-            const int k = (o - p.d_c) >> 1;
-            const size_t t = static_cast<size_t>(ss->tpos[c0 + col]) * half + k;
-            const float cs = __ldg(p.rope_cos + t), sn = __ldg(p.rope_sin + t);
-            store_pair(dst, acc.x * cs - acc.y * sn, acc.x * sn + acc.y * cs);
+            const int o = (o_tile % p.tiles_per_group) * kBM + row;  // latent column of head `group`
+            if (o < p.out)
+              store_pair(p.q_lat + (static_cast<size_t>(n) * p.n_h + group) * p.width + o, a.x, a.y);
           }
-        } else {
-          const int o = (o_tile % p.tiles_per_group) * kBM + row;  // latent column of head `group`
-          if (o < p.out)
-            store_pair(p.q_lat + (static_cast<size_t>(n) * p.n_h + group) * p.width + o, acc.x, acc.y);
         }
       }
     }
@@ -291,44 +331,70 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
       __syncthreads();
     }
   }
-  if (MODE == kModeAbsorb && ok && split == 0) {
+  if (MODE == kModeAbsorb && ok) {
     // the positional part of the latent query: RoPE_pos(q^R_i) ([qiita] "RoPE の扱い"),
-    // shared out over the head's output tiles; every load of an item is
-    // independent of the others, so they all go out before any is used
-    const int m = o_tile % p.tiles_per_group, nm = p.tiles_per_group;
+    // shared out over the CTAs of the head; each thread gathers the operands
+    // of a batch of items before using any, so their loads overlap
+    const int m = ((tile0 % p.tiles_per_group) / MT) * nsplit + split, nm = (p.tiles_per_group / MT) * nsplit;
     const int items = NT * half;
-    for (int f = threadIdx.x + kThreads * m; f < items; f += kThreads * nm) {
-      const int n = n0 + f / half, k = f % half;
-      if (n >= p.n_tok) continue;
-      const int tp = __ldg(p.pos + n);
-      const size_t hn = static_cast<size_t>(n) * p.n_h + group;
-      const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(p.q_r + hn * p.d_hr + 2 * k);
-      if (tp < 0 || tp >= p.max_pos) {
-        report(p.status, MLA_ERR_DEVICE_BOUNDS);
-        continue;
+    constexpr int kBatch = 8;
+    const int stride = kThreads * nm;
+    for (int base = threadIdx.x + kThreads * m; base < items; base += stride * kBatch) {
+      int tp[kBatch];
+      __nv_bfloat162 x[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int f = base + b * stride;
+        const int n = n0 + f / half, k = f % half;
+        const bool live = f < items && n < p.n_tok;
+        tp[b] = live ? __ldg(p.pos + n) : -1;
+        x[b] = live ? *reinterpret_cast<const __nv_bfloat162*>(p.q_r + (static_cast<size_t>(n) * p.n_h + group) * p.d_hr + 2 * k)
+                    : __nv_bfloat162();
       }
-      const size_t t = static_cast<size_t>(tp) * half + k;
-      const float cs = __ldg(p.rope_cos + t), sn = __ldg(p.rope_sin + t);
-      const float x0 = __bfloat162float(x.x), x1 = __bfloat162float(x.y);
-      store_pair(p.q_lat + hn * p.width + p.d_c + 2 * k, x0 * cs - x1 * sn, x0 * sn + x1 * cs);
+      float cs[kBatch], sn[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int f = base + b * stride, k = f % half;
+        const bool live = tp[b] >= 0 && tp[b] < p.max_pos;
+        const size_t t = live ? static_cast<size_t>(tp[b]) * half + k : 0;
+        cs[b] = live ? __ldg(p.rope_cos + t) : 0.f;
+        sn[b] = live ? __ldg(p.rope_sin + t) : 0.f;
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int f = base + b * stride;
+        const int n = n0 + f / half, k = f % half;
+        if (f >= items || n >= p.n_tok) continue;
+        if (tp[b] < 0 || tp[b] >= p.max_pos) {
+          report(p.status, MLA_ERR_DEVICE_BOUNDS);
+          continue;
+        }
+        const float x0 = __bfloat162float(x[b].x), x1 = __bfloat162float(x[b].y);
+        const size_t hn = static_cast<size_t>(n) * p.n_h + group;
+        store_pair(p.q_lat + hn * p.width + p.d_c + 2 * k, x0 * cs[b] - x1 * sn[b], x0 * sn[b] + x1 * cs[b]);
+      }
     }
   }
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, NT);
+    tmem_dealloc(tmem, NT * MT);
   }
 }
 
-template <int NT, int STAGES, int MODE>
-cudaError_t launch_proj_nt(const ProjMaps& maps, const ProjParams& p, int nsplit, int o_tiles, int n_tiles,
+template <int NT, int STAGES, int MODE, int MT>
+cudaError_t launch_proj_nt(const ProjMaps& maps, const ProjParams& p, int nsplit, int tile_groups, int n_tiles,
                            cudaStream_t s) {
   constexpr size_t kSmem = STAGES * (kABytes + NT * kBK * 2) + sizeof(ProjShared<STAGES, NT>) + 1024;
-  auto kern = proj_kernel<NT, STAGES, MODE>;
+  auto kern = proj_kernel<NT, STAGES, MODE, MT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
   if (e != cudaSuccess) return e;
+  if (nsplit > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nsplit, o_tiles, n_tiles);
+  cfg.gridDim = dim3(nsplit, tile_groups, n_tiles);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = s;
@@ -344,23 +410,25 @@ cudaError_t launch_proj_nt(const ProjMaps& maps, const ProjParams& p, int nsplit
 
 // Token-tile width: the smallest of 64/128/256 that holds every token, else
 // 256-token tiles.  Stages: enough for ~100-150 KB of loads in flight.
-template <int MODE>
+template <int MODE, int MT>
 cudaError_t launch_proj(const ProjMaps& maps, const ProjParams& p, int nsplit, int o_tiles, cudaStream_t s) {
-  if (p.n_tok <= 64) return launch_proj_nt<64, 4, MODE>(maps, p, nsplit, o_tiles, 1, s);
-  if (p.n_tok <= 128) return launch_proj_nt<128, 4, MODE>(maps, p, nsplit, o_tiles, 1, s);
-  return launch_proj_nt<256, 3, MODE>(maps, p, nsplit, o_tiles, (p.n_tok + 255) / 256, s);
+  const int groups = o_tiles / MT;
+  if (p.n_tok <= 64) return launch_proj_nt<64, 4, MODE, MT>(maps, p, nsplit, groups, 1, s);
+  if (p.n_tok <= 128) return launch_proj_nt<128, 4, MODE, MT>(maps, p, nsplit, groups, 1, s);
+  return launch_proj_nt<256, 3, MODE, (MT > 2 ? 2 : MT)>(maps, p, nsplit, o_tiles / (MT > 2 ? 2 : MT),
+                                                        (p.n_tok + 255) / 256, s);
 }
 
 int token_tile(int n_tok) { return n_tok <= 64 ? 64 : n_tok <= 128 ? 128 : 256; }
 
-// k-range split so that about two CTAs per SM (one for wide token tiles) stream weights.
-int pick_split(const mla_handle* h, int o_tiles, int n_tok, int k_blocks) {
+// k-range split: the largest that keeps the grid within one wave (two CTAs
+// per SM for 64-token tiles, one otherwise) and gives every CTA a k block.
+int pick_split(const mla_handle* h, int ctas_per_split, int n_tok, int k_blocks) {
   const int nt = token_tile(n_tok);
-  const long long base = static_cast<long long>(o_tiles) * ((n_tok + nt - 1) / nt);
-  const long long target = static_cast<long long>(h->num_sms) * (nt == 64 ? 2 : 1);
-  // the largest power of two that keeps the grid within about one wave
+  const long long base = static_cast<long long>(ctas_per_split) * ((n_tok + nt - 1) / nt);
+  const long long slots = static_cast<long long>(h->num_sms) * (nt == 64 ? 2 : 1);
   int sp = 1;
-  while (sp * 2 <= kMaxSplit && sp * 2 <= k_blocks && base * sp * 2 <= target + target / 8) sp *= 2;
+  while (sp + 1 <= kMaxSplit && sp + 1 <= k_blocks && base * (sp + 1) <= slots) ++sp;
   return sp;
 }
 
@@ -416,6 +484,7 @@ cudaError_t launch_linear_tc(const mla_handle* h, const void* X, int x_cols, con
   const int nt = token_tile(n_tok);
   if (!encode_bf16_2d(&maps.w, W, in, out, kBK, kBM) || !encode_bf16_2d(&maps.x, X, x_cols, n_tok, kBK, nt))
     return cudaErrorInvalidValue;
+  maps.w2 = maps.w;
   ProjParams p = base_params(h, n_tok);
   const int o_tiles = (out + kBM - 1) / kBM;
   p.out = out;
@@ -424,7 +493,29 @@ cudaError_t launch_linear_tc(const mla_handle* h, const void* X, int x_cols, con
   p.x_group_cols = groups > 1 ? x_group_cols : 0;
   p.y = static_cast<__nv_bfloat16*>(Y);
   p.ldy = ldy;
-  return launch_proj<kModeLinear>(maps, p, pick_split(h, o_tiles, n_tok, p.k_blocks), o_tiles, s);
+  p.seg1_tiles = 1 << 30;
+  return launch_proj<kModeLinear, 1>(maps, p, pick_split(h, o_tiles, n_tok, p.k_blocks), o_tiles, s);
+}
+
+cudaError_t launch_linear2_tc(const mla_handle* h, const void* X, int in, const void* W1, int out1, void* Y1,
+                              long long ldy1, const void* W2, int out2, void* Y2, long long ldy2, int n_tok,
+                              cudaStream_t s) {
+  ProjMaps maps;
+  const int nt = token_tile(n_tok);
+  if (!encode_bf16_2d(&maps.w, W1, in, out1, kBK, kBM) || !encode_bf16_2d(&maps.w2, W2, in, out2, kBK, kBM) ||
+      !encode_bf16_2d(&maps.x, X, in, n_tok, kBK, nt))
+    return cudaErrorInvalidValue;
+  ProjParams p = base_params(h, n_tok);
+  const int t1 = (out1 + kBM - 1) / kBM, t2 = (out2 + kBM - 1) / kBM;
+  p.out = out1;
+  p.out2 = out2;
+  p.k_blocks = (in + kBK - 1) / kBK;
+  p.y = static_cast<__nv_bfloat16*>(Y1);
+  p.ldy = ldy1;
+  p.y2 = static_cast<__nv_bfloat16*>(Y2);
+  p.ldy2 = ldy2;
+  p.seg1_tiles = t1;
+  return launch_proj<kModeLinear, 1>(maps, p, pick_split(h, t1 + t2, n_tok, p.k_blocks), t1 + t2, s);
 }
 
 cudaError_t launch_cache_append_tc(const mla_handle* h, const void* x, const void* w_dkr, const int* seq_idx,
@@ -447,7 +538,9 @@ cudaError_t launch_cache_append_tc(const mla_handle* h, const void* x, const voi
   p.batch = batch;
   p.n_pool_blocks = n_pool_blocks;
   p.pool = static_cast<__nv_bfloat16*>(pool);
-  return launch_proj<kModeAppend>(maps, p, pick_split(h, o_tiles, n_new, p.k_blocks), o_tiles, s);
+  maps.w2 = maps.w;
+  p.seg1_tiles = 1 << 30;
+  return launch_proj<kModeAppend, 1>(maps, p, pick_split(h, o_tiles, n_new, p.k_blocks), o_tiles, s);
 }
 
 cudaError_t launch_absorb_q_tc(const mla_handle* h, const void* q_c, const void* q_r, const int* pos, int n_tok,
@@ -468,7 +561,13 @@ cudaError_t launch_absorb_q_tc(const mla_handle* h, const void* q_c, const void*
   p.pos = pos;
   p.q_lat = static_cast<__nv_bfloat16*>(q_lat);
   p.q_r = static_cast<const __nv_bfloat16*>(q_r);
-  return launch_proj<kModeAbsorb>(maps, p, 1, per_head * d.n_h, s);
+  maps.w2 = maps.w;
+  p.seg1_tiles = 1 << 30;
+  // all of a head's output tiles in one CTA (they share the q^C tile)
+  constexpr int kMT = 4;
+  if (per_head % kMT != 0) return cudaErrorInvalidValue;
+  // d_h = 128 is two k blocks: no split, so no cluster reduction
+  return launch_proj<kModeAbsorb, kMT>(maps, p, 1, per_head * d.n_h, s);
 }
 
 }  // namespace mla
