@@ -244,6 +244,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_wait();
   tc_fence_after();
   const uint32_t tmem = bs->tmem_base;
+  pdl_wait();  // the plan, the latent queries and the cache rows are written by earlier kernels
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -597,6 +598,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
+  if (threadIdx.x == 0) pdl_trigger();
   cluster_arrive();  // no CTA leaves while its peer may still touch its shared memory
   cluster_wait();
   if (warp == 1) {
@@ -611,6 +613,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ seq_
                                                     int* status) {
   __shared__ int warp_sums[32];
   __shared__ int carry;
+  if (threadIdx.x == 0) pdl_trigger();  // the decode CTAs may set up meanwhile
+  pdl_wait();
   if (threadIdx.x == 0) { carry = 0; prefix[0] = 0; }
   if (threadIdx.x == 0 && __ldg(cu_q + batch) != n_tok) report(status, MLA_ERR_DEVICE_BOUNDS);
   __syncthreads();
@@ -671,6 +675,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const int* __restrict__ pr
                                                       const float* __restrict__ part_o,
                                                       const float* __restrict__ part_lse,
                                                       __nv_bfloat16* __restrict__ o_lat, float* __restrict__ lse) {
+  if (threadIdx.x == 0) pdl_trigger();
+  pdl_wait();
   const int n = blockIdx.x;
   const int total = __ldg(prefix + n_tok);
   const int t0 = __ldg(prefix + n), t1 = __ldg(prefix + n + 1);
@@ -752,6 +758,21 @@ bool encode_pool_map(CUtensorMap* m, const void* pool, long long rows, uint32_t 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// plan -> decode -> combine, each allowed to launch while its predecessor finishes.
+cudaError_t launch_decode_kernels(const Maps& maps, const Params& prm, int W, int n_tok, const int* seq_lens,
+                                  const int* cu_q, int batch, int max_blocks, float* lse, int* status, cudaStream_t s) {
+  cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s, 1, seq_lens, cu_q, batch, n_tok, max_blocks,
+                             const_cast<int*>(prm.prefix), status);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(decode_tc_kernel, dim3(2 * W), dim3(kThreads), kSmemBytes, s, 1, maps, prm);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(combine_kernel, dim3(n_tok, kHeads / 8), dim3(256), 0, s, 1, static_cast<const int*>(prm.prefix),
+                    n_tok, W, static_cast<const float*>(prm.part_o), static_cast<const float*>(prm.part_lse), prm.o_lat,
+                    lse);
+}
+
 int resolve_workers(const mla_handle* h, int num_workers) {
   return num_workers > 0 ? num_workers : max(1, h->num_sms / 2);
 }
@@ -798,20 +819,7 @@ cudaError_t launch_decode_tc(const mla_handle* h, const void* q_lat, const void*
   prm.workers = W;
   prm.scale_log2 = h->dims.scale * kLog2e;
 
-  plan_kernel<<<1, 1024, 0, s>>>(seq_lens, cu_q, batch, n_tok, max_blocks, const_cast<int*>(prm.prefix), h->status);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  decode_tc_kernel<<<2 * W, kThreads, kSmemBytes, s>>>(maps, prm);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  combine_kernel<<<dim3(n_tok, kHeads / 8), 256, 0, s>>>(prm.prefix, n_tok, W, prm.part_o, prm.part_lse, prm.o_lat, lse);
-  return cudaGetLastError();
+  return launch_decode_kernels(maps, prm, W, n_tok, seq_lens, cu_q, batch, max_blocks, lse, h->status, s);
 }
 
 
@@ -912,13 +920,9 @@ int launch_decode_tc_noalloc(const mla_handle* h, const void* q_lat, const void*
   prm.n_pool_blocks = n_pool_blocks;
   prm.workers = W;
   prm.scale_log2 = h->dims.scale * kLog2e;
-  plan_kernel<<<1, 1024, 0, s>>>(seq_lens, cu_q, batch, n_tok, max_blocks, const_cast<int*>(prm.prefix), h->status);
-  if (cudaGetLastError() != cudaSuccess) return 2;
-  if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
-    return 2;
-  decode_tc_kernel<<<2 * W, kThreads, kSmemBytes, s>>>(maps, prm);
-  if (cudaGetLastError() != cudaSuccess) return 2;
-  combine_kernel<<<dim3(n_tok, kHeads / 8), 256, 0, s>>>(prm.prefix, n_tok, W, prm.part_o, prm.part_lse, prm.o_lat, lse);
-  return cudaGetLastError() == cudaSuccess ? 0 : 2;
+  return launch_decode_kernels(maps, prm, W, n_tok, seq_lens, cu_q, batch, max_blocks, lse, h->status, s) ==
+                 cudaSuccess
+             ? 0
+             : 2;
 }
 }  // namespace mla

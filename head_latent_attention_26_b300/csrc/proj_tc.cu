@@ -157,29 +157,41 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
       tma_prefetch_desc(&maps.x);
       const uint64_t pol_w = l2_policy_evict_first(), pol_x = l2_policy_evict_last();
       const int x_off = group * p.x_group_cols;
-      uint32_t it = 0;
-      bool go = true;
-      for (int mi = 0; mi < MT && go; ++mi) {
-        const int o_tile = tile0 + mi;
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int s = it % STAGES;
-          if (it >= STAGES && !proj_wait(&ss->empty[s], ((it / STAGES) - 1) & 1, p, &ss->abort)) {
-            go = false;
-            break;
-          }
-          uint8_t* st = smem + s * kStage;
-          mbar_arrive_expect_tx(&ss->full[s], kStage);
-          if (MODE == kModeAbsorb) {
-            // W^UK_i^T tile: 64 rows of head i (the k side) x 128 latent columns (the M side)
-            const int m = o_tile % p.tiles_per_group;
-            const int y = group * p.w_group_rows + kb * kBK;
-            tma_load_2d_hint(st, wmap, &ss->full[s], m * kBM, y, pol_w);
-            tma_load_2d_hint(st + kABytes / 2, wmap, &ss->full[s], m * kBM + 64, y, pol_w);
-          } else {
-            tma_load_2d_hint(st, wmap, &ss->full[s], kb * kBK, o_tile * kBM, pol_w);
-          }
-          tma_load_2d_hint(st + kABytes, &maps.x, &ss->full[s], x_off + kb * kBK, n0, pol_x);
+      // The weights do not depend on earlier kernels: the first STAGES weight
+      // tiles go out before the wait for the previous kernel, their token
+      // tiles right after it.
+      const int n_loads = MT * (kb1 - kb0);
+      const int early = n_loads < STAGES ? n_loads : STAGES;
+      auto load_w = [&](int i, uint8_t* st, uint64_t* bar) {
+        const int o_tile = tile0 + i / (kb1 - kb0), kb = kb0 + i % (kb1 - kb0);
+        if (MODE == kModeAbsorb) {
+          // W^UK_i^T tile: 64 rows of head i (the k side) x 128 latent columns (the M side)
+          const int m = o_tile % p.tiles_per_group;
+          const int y = group * p.w_group_rows + kb * kBK;
+          tma_load_2d_hint(st, wmap, bar, m * kBM, y, pol_w);
+          tma_load_2d_hint(st + kABytes / 2, wmap, bar, m * kBM + 64, y, pol_w);
+        } else {
+          tma_load_2d_hint(st, wmap, bar, kb * kBK, o_tile * kBM, pol_w);
         }
+      };
+      auto load_x = [&](int i, uint8_t* st, uint64_t* bar) {
+        const int kb = kb0 + i % (kb1 - kb0);
+        tma_load_2d_hint(st + kABytes, &maps.x, bar, x_off + kb * kBK, n0, pol_x);
+      };
+      for (int i = 0; i < early; ++i) {
+        mbar_arrive_expect_tx(&ss->full[i], kStage);
+        load_w(i, smem + i * kStage, &ss->full[i]);
+      }
+      pdl_wait();
+      for (int i = 0; i < early; ++i) load_x(i, smem + i * kStage, &ss->full[i]);
+      uint32_t it = early;
+      for (int i = early; i < n_loads; ++i, ++it) {
+        const int s = it % STAGES;
+        if (!proj_wait(&ss->empty[s], ((it / STAGES) - 1) & 1, p, &ss->abort)) break;
+        uint8_t* st = smem + s * kStage;
+        mbar_arrive_expect_tx(&ss->full[s], kStage);
+        load_w(i, st, &ss->full[s]);
+        load_x(i, st, &ss->full[s]);
       }
       if (ss->abort) {
         // every issued copy must land before the CTA may exit
@@ -220,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     }
   } else if (MODE == kModeAppend) {
     // ---------------------------------------------------------------- destination rows
+    pdl_wait();
     for (int j = threadIdx.x - 64; j < NT; j += 64) {
       const int n = n0 + j;
       int slot = -1, tp = 0;
@@ -243,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
   // -------------------------------------------------------------------- epilogue
   bool ok = proj_wait(&ss->done, 0, p, &ss->abort) && !*reinterpret_cast<volatile int*>(&ss->abort);
   tc_fence_after();
+  if (threadIdx.x == 0) pdl_trigger();  // every CTA of this grid is resident: the next may launch
   float* red = reinterpret_cast<float*>(smem);  // [64 columns][128 rows] fp32, stages reused
   const uint32_t red_addr = smem_u32(red);
   const int r = warp * 32 + lane;  // TMEM lane = output row of the tile
@@ -393,19 +407,7 @@ cudaError_t launch_proj_nt(const ProjMaps& maps, const ProjParams& p, int nsplit
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nsplit, tile_groups, n_tiles);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmem;
-  cfg.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = nsplit;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, maps, p);
+  return launch_pdl(kern, dim3(nsplit, tile_groups, n_tiles), dim3(kThreads, 1, 1), kSmem, s, nsplit, maps, p);
 }
 
 // Token-tile width: the smallest of 64/128/256 that holds every token, else

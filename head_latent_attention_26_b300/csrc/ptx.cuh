@@ -57,6 +57,15 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Kernels of the library are launched so that the next kernel in the stream
+// may start while this one finishes.  Every kernel waits (pdl_wait) before it
+// reads anything an earlier kernel wrote or writes anything an earlier kernel
+// reads, and lets its successor launch (pdl_trigger) once its own CTAs no
+// longer need to be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ cluster
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
