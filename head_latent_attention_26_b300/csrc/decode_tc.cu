@@ -68,7 +68,6 @@ constexpr int kWidth = 576;             // d_c + d_hr
 constexpr int kDc = 512;
 constexpr int kStages = 5;             // latent stages (32 KB each)
 constexpr int kRopeSlots = 3;          // RoPE boxes live only until their score MMA
-constexpr int kPrefetchTiles = 6;      // tiles pulled into L2 ahead of the stage loads
 constexpr uint32_t kBoxBytes = kTile * 128;                 // 64 keys x 64 cols bf16 (128B swizzle)
 constexpr uint32_t kRopeBoxBytes = kTile * 64;              // 64 keys x 32 cols bf16 (64B swizzle)
 constexpr uint32_t kStageBytes = 4 * kBoxBytes;             // 32768: the latent columns of a tile
@@ -262,24 +261,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         return blk * kBlockRows;
       };
-      // A second cursor walks kPrefetchTiles ahead and pulls those tiles into
-      // L2, so the loads into the (few) shared-memory stages see L2 latency.
-      UnitIter pit = make_iter(p, g);
-      Unit pu;
-      bool pvalid = pit.next(p, g, pu);
-      int pt = pvalid ? pu.ta : 0;
-      auto prefetch_next = [&]() {
-        if (!pvalid) return;
-        const int y = tile_row(pu.b, pt);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) tma_prefetch_l2_2d(&maps.latent, 256 * c + 64 * j, y);
-        tma_prefetch_l2_2d(&maps.rope, 512 + 32 * c, y);
-        if (++pt >= pu.tb) {
-          pvalid = pit.next(p, g, pu);
-          if (pvalid) pt = pu.ta;
-        }
-      };
-      for (int i = 0; i < kPrefetchTiles; ++i) prefetch_next();
       UnitIter iter = make_iter(p, g);
       Unit u;
       uint32_t it = 0;
@@ -298,7 +279,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 4; ++j)
             tma_load_2d_hint(st + j * kBoxBytes, &maps.latent, &bs->full[s], 256 * c + 64 * j, y, pol);
           tma_load_2d_hint(smem + kOffRope + rs * kRopeBoxBytes, &maps.rope, &bs->full[s], 512 + 32 * c, y, pol);
-          prefetch_next();
         }
       }
       // drain: every issued stage must land before the CTA may exit
