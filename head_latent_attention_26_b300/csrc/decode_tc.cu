@@ -32,9 +32,13 @@
 //   (M=128, N=256, K=64) in TMEM, with P (bf16) in TMEM and the key tile read
 //   again from the same shared-memory stage as an MN-major B operand.  No K or
 //   V is ever expanded.
-// * The MMA issuer computes S two tiles ahead of the softmax: while the row
-//   warps turn tile t into probabilities they hold S(t+1) in registers and the
-//   tensor pipe runs O(t-1) and S(t+2) (one TMEM buffer for S is enough).
+// * Two warps issue the MMAs: one the scores, one the values.  A tcgen05.mma
+//   issue stalls while the tensor pipe's queue is full, so a single issuer
+//   busy pushing an 18-MMA score batch could not see that P is ready; with two
+//   issuers each kind goes in as soon as its inputs are.  S runs ahead of the
+//   softmax: while the row warps turn tile t into probabilities they hold
+//   S(t+1) in registers and the tensor pipe runs O(t-1) and S(t+2) (one TMEM
+//   buffer for S is enough).
 // * Rescaling of O is lazy: the running max only moves when a tile's max
 //   exceeds it by more than 2^8, which keeps every exp2 argument <= 8 and the
 //   result exact (numerator and denominator share the stale max).
@@ -42,9 +46,10 @@
 //   the global tile list); split pieces write fp32 partials that a separate
 //   log-sum-exp combine kernel merges.
 //
-// Warp roles per CTA (192 threads): warp 0 = TMA producer, warp 1 = MMA
-// issuer + TMEM owner (the whole warp runs the loop, one elected lane issues
-// each batch of MMAs), warps 2..5 = "row" warps, thread = head (TMEM lane).
+// Warp roles per CTA (224 threads): warp 0 = TMA producer, warp 1 = score
+// MMA issuer + TMEM owner, warp 6 = value MMA issuer (each issuer runs its
+// loop as a whole warp, one elected lane issues each batch of MMAs), warps
+// 2..5 = "row" warps, thread = head (TMEM lane).
 // Every wait is bounded; a wait that runs out records MLA_ERR_DEVICE_TIMEOUT,
 // raises a CTA-wide abort flag and the roles drain and exit.
 #include <cuda.h>
@@ -83,7 +88,8 @@ constexpr uint32_t kSmemBytes = kOffBars + 512 + 1024;      // + alignment slack
 // TMEM columns (512 allocated): O half | Q~ latent half | Q~ RoPE half | P | S
 // (bf16 operands hold two elements per 32-bit column)
 constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemQR = 384, kTmemP = 416, kTmemS = 448;
-constexpr int kThreads = 64 + 32 * kRowWarps;
+constexpr int kThreads = 64 + 32 * kRowWarps + 32;
+constexpr int kValueWarp = 2 + kRowWarps;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -113,7 +119,7 @@ struct Bars {
   uint64_t q_ready, s_full, s_free, p_ready, p_free;
   uint64_t xin_full[2][kRowWarps];    // peer warp w's partial scores landed in inbox slot
   uint64_t inbox_free[2][kRowWarps];  // peer warp w has consumed the slot this CTA writes into
-  uint64_t drain;
+  uint64_t drain, drain_o;
   uint32_t tmem_base;
   int abort;
 };
@@ -228,6 +234,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(&bs->inbox_free[s][w], 1);
       }
     mbar_init(&bs->drain, 1);
+    mbar_init(&bs->drain_o, 1);
     bs->abort = 0;
     fence_mbar_init();
     // first phase of every inbox barrier: one arrival (this one) + the bytes
@@ -289,57 +296,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ score MMA issuer
     // The whole warp runs this loop (operands stay warp-uniform); one elected
-    // lane issues each tcgen05 instruction.
+    // lane issues each batch of MMAs.
     {
       const uint32_t idesc_s = idesc_bf16_f32(128, kTile, false, false);
-      const uint32_t idesc_o = idesc_bf16_f32(128, 256, false, true);
       UnitIter iter = make_iter(p, g);
       Unit u;
-      uint32_t n_sq = 0;     // S tiles issued (global); tile k sits in stage k % kStages
-      uint32_t n_o = 0;      // O MMAs issued (global)
+      uint32_t k = 0;  // S tiles issued (global); tile k sits in stage k % kStages
       uint32_t n_units = 0;
       bool ok = true;
-      // S(k) into the single S buffer once the row warps have read S(k-1) out of it
-      auto issue_s = [&]() -> bool {
-        const uint32_t k = n_sq;
-        if (!wait_bar_warp(&bs->full[k % kStages], (k / kStages) & 1, p, bs)) return false;
-        if (k >= 1 && !wait_bar_warp(&bs->s_free, (k - 1) & 1, p, bs)) return false;
-        tc_fence_after();
-        const uint32_t st = smem_u32(smem + kOffStages + (k % kStages) * kStageBytes);
-        const uint32_t rope = smem_u32(smem + kOffRope + (k % kRopeSlots) * kRopeBoxBytes);
-        mma_score_tile_elect<kBoxBytes>(tmem + kTmemS, tmem + kTmemQ, tmem + kTmemQR, smem_desc(st, 16, 1024, kSwizzle128B),
-                                        smem_desc(rope, 16, 512, kSwizzle64B), idesc_s);
-        mma_commit_elect(&bs->s_full);
-        mma_commit_elect(&bs->rope_empty[k % kRopeSlots]);
-        ++n_sq;
-        return true;
-      };
       while (ok && iter.next(p, g, u)) {
         ok = wait_bar_warp(&bs->q_ready, n_units & 1, p, bs);
         ++n_units;
         if (!ok) break;
         tc_fence_after();
-        const uint32_t n = static_cast<uint32_t>(u.tb - u.ta), it0 = n_sq;
-        if (!(ok = issue_s())) break;
-        if (n > 1 && !(ok = issue_s())) break;
-        for (uint32_t t = 0; t < n && ok; ++t) {
-          if (t + 2 < n && !(ok = issue_s())) break;  // waits until the row warps hold S(t+1)
-          if (!(ok = wait_bar_warp(&bs->p_ready, n_o & 1, p, bs))) break;
+        for (int t = u.ta; t < u.tb && ok; ++t, ++k) {
+          // S(k) into the single S buffer once the row warps have read S(k-1) out of it
+          if (!(ok = wait_bar_warp(&bs->full[k % kStages], (k / kStages) & 1, p, bs))) break;
+          if (k >= 1 && !(ok = wait_bar_warp(&bs->s_free, (k - 1) & 1, p, bs))) break;
           tc_fence_after();
-          const uint32_t st = smem_u32(smem + kOffStages + ((it0 + t) % kStages) * kStageBytes);
-          mma_value_tile_elect<kTile / 16>(tmem + kTmemO, tmem + kTmemP, smem_desc(st, kBoxBytes, 1024, kSwizzle128B),
-                                           idesc_o, t > 0 ? 1u : 0u);
-          mma_commit_elect(&bs->p_free);
-          mma_commit_elect(&bs->empty[(it0 + t) % kStages]);
-          ++n_o;
+          const uint32_t st = smem_u32(smem + kOffStages + (k % kStages) * kStageBytes);
+          const uint32_t rope = smem_u32(smem + kOffRope + (k % kRopeSlots) * kRopeBoxBytes);
+          mma_score_tile_elect<kBoxBytes>(tmem + kTmemS, tmem + kTmemQ, tmem + kTmemQR,
+                                          smem_desc(st, 16, 1024, kSwizzle128B),
+                                          smem_desc(rope, 16, 512, kSwizzle64B), idesc_s);
+          mma_commit_elect(&bs->s_full);
+          mma_commit_elect(&bs->rope_empty[k % kRopeSlots]);
         }
       }
       if (!ok) {
         // every issued MMA must finish before TMEM is released
         mma_commit_elect(&bs->drain);
         for (long long i = 0; i < p.wait_limit && !mbar_try_wait(&bs->drain, 0); ++i) {
+        }
+      }
+    }
+  } else if (warp == kValueWarp) {
+    // ------------------------------------------------------------ value MMA issuer
+    {
+      const uint32_t idesc_o = idesc_bf16_f32(128, 256, false, true);
+      UnitIter iter = make_iter(p, g);
+      Unit u;
+      uint32_t k = 0;  // O MMAs issued (global)
+      bool ok = true;
+      while (ok && iter.next(p, g, u)) {
+        for (int t = u.ta; t < u.tb && ok; ++t, ++k) {
+          // P(k) is in TMEM (and S(k) done, so the stage has landed)
+          if (!(ok = wait_bar_warp(&bs->p_ready, k & 1, p, bs))) break;
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + kOffStages + (k % kStages) * kStageBytes);
+          mma_value_tile_elect<kTile / 16>(tmem + kTmemO, tmem + kTmemP, smem_desc(st, kBoxBytes, 1024, kSwizzle128B),
+                                           idesc_o, t > u.ta ? 1u : 0u);
+          mma_commit_elect(&bs->p_free);
+          mma_commit_elect(&bs->empty[k % kStages]);
+        }
+      }
+      if (!ok) {
+        mma_commit_elect(&bs->drain_o);
+        for (long long i = 0; i < p.wait_limit && !mbar_try_wait(&bs->drain_o, 0); ++i) {
         }
       }
     }

@@ -27,7 +27,7 @@ struct mla_handle {
 
 namespace mla {
 
-constexpr long long kDefaultWaitLimit = 1ll << 26;  // mbarrier polls before giving up
+constexpr long long kDefaultWaitLimit = 1ll << 24;  // mbarrier polls (about 0.1 us each) before giving up
 
 // Records `code` in the status word unless an earlier error is already there.
 __device__ __forceinline__ void report(int* status, int code) { atomicCAS(status, 0, code); }

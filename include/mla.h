@@ -90,7 +90,8 @@ int mla_num_sms(const mla_handle* h);
 int mla_uses_tensor_path(const mla_handle* h);
 
 /* Upper bound, in device polls, on every bounded wait of later launches
- * (0 = library default). Used to exercise the timeout path. */
+ * (0 = library default, 2^24 polls of roughly 0.1 us each, about 2 s).
+ * Used to exercise the timeout path. */
 mla_status mla_set_wait_limit(mla_handle* h, long long polls);
 
 /* ---- a0: query projection --------------------------------------------------
