@@ -553,33 +553,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = 1.f / l;
       const float lse_val = (m + log2f(l)) * 0.69314718055994531f;
+      // Rows leave TMEM one head per thread; each 32-column chunk goes through
+      // this warp's (idle) outbox block so that every global store instruction
+      // covers whole row segments of 4 heads (fp32) or 8 heads (bf16) instead
+      // of 32 scattered 16-byte pieces.
+      if (lane == 0) bulk_wait_read<0>();  // no copy still reads the outbox
+      __syncwarp();
+      uint8_t* const stg = outbox;         // 32 rows x 128 B
+      const size_t row0 = static_cast<size_t>(u.slot < 0 ? u.n : u.slot) * kHeads + q * 32;  // first head of the warp
       if (u.slot < 0) {
-        __nv_bfloat16* dst = p.o_lat + (static_cast<size_t>(u.n) * kHeads + r) * kDc + 256 * c;
+        __nv_bfloat16* const dst = p.o_lat + row0 * kDc + 256 * c;
 #pragma unroll 1
-        for (int ch = 0; ch < 16; ++ch) {
-          uint32_t v[16];
-          tmem_ld16(tmem + lane_base + kTmemO + ch * 16, v);
-          tmem_ld_wait();
-          uint32_t o[8];
+        for (int ch = 0; ch < 8; ++ch) {
+          uint8_t* const wrow = stg + lane * 64;  // 32 bf16 = 64 B per head
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            o[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * inv_l, __uint_as_float(v[2 * j + 1]) * inv_l);
-          reinterpret_cast<uint4*>(dst + ch * 16)[0] = make_uint4(o[0], o[1], o[2], o[3]);
-          reinterpret_cast<uint4*>(dst + ch * 16)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t v[16];
+            tmem_ld16(tmem + lane_base + kTmemO + ch * 32 + hf * 16, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+              const int k = 2 * hf + kk;
+              uint32_t o[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                o[j] = pack_bf16x2(__uint_as_float(v[8 * kk + 2 * j]) * inv_l, __uint_as_float(v[8 * kk + 2 * j + 1]) * inv_l);
+              *reinterpret_cast<uint4*>(wrow + ((k ^ ((lane >> 1) & 3)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int row = 8 * i + (lane >> 2), k = lane & 3;
+            const uint4 w = *reinterpret_cast<const uint4*>(stg + row * 64 + ((k ^ ((row >> 1) & 3)) * 16));
+            *reinterpret_cast<uint4*>(dst + static_cast<size_t>(row) * kDc + ch * 32 + k * 8) = w;
+          }
+          __syncwarp();
         }
         if (c == 0) p.lse[static_cast<size_t>(u.n) * kHeads + r] = lse_val;
       } else {
-        float* dst = p.part_o + (static_cast<size_t>(u.slot) * kHeads + r) * kDc + 256 * c;
+        float* const dst = p.part_o + row0 * kDc + 256 * c;
 #pragma unroll 1
-        for (int ch = 0; ch < 16; ++ch) {
-          uint32_t v[16];
-          tmem_ld16(tmem + lane_base + kTmemO + ch * 16, v);
-          tmem_ld_wait();
+        for (int ch = 0; ch < 8; ++ch) {
+          uint8_t* const wrow = stg + lane * 128;  // 32 fp32 = 128 B per head
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            reinterpret_cast<float4*>(dst + ch * 16)[j] =
-                make_float4(__uint_as_float(v[4 * j]) * inv_l, __uint_as_float(v[4 * j + 1]) * inv_l,
-                            __uint_as_float(v[4 * j + 2]) * inv_l, __uint_as_float(v[4 * j + 3]) * inv_l);
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t v[16];
+            tmem_ld16(tmem + lane_base + kTmemO + ch * 32 + hf * 16, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const int k = 4 * hf + kk;
+              *reinterpret_cast<float4*>(wrow + ((k ^ (lane & 7)) * 16)) =
+                  make_float4(__uint_as_float(v[4 * kk]) * inv_l, __uint_as_float(v[4 * kk + 1]) * inv_l,
+                              __uint_as_float(v[4 * kk + 2]) * inv_l, __uint_as_float(v[4 * kk + 3]) * inv_l);
+            }
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int row = 4 * i + (lane >> 3), k = lane & 7;
+            const float4 w = *reinterpret_cast<const float4*>(stg + row * 128 + ((k ^ (row & 7)) * 16));
+            *reinterpret_cast<float4*>(dst + static_cast<size_t>(row) * kDc + ch * 32 + k * 4) = w;
+          }
+          __syncwarp();
         }
         if (c == 0) p.part_lse[static_cast<size_t>(u.slot) * kHeads + r] = lse_val;
       }
