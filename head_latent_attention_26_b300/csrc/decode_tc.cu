@@ -116,7 +116,10 @@ struct Params {
 
 struct Bars {
   uint64_t full[kStages], empty[kStages], rope_empty[kRopeSlots];
-  uint64_t q_ready, s_full, s_free, p_ready, p_free;
+  uint64_t s_full, p_free;
+  // progress counters of the row warps, polled by the MMA issuers: query
+  // tokens loaded into TMEM, S tiles read out of TMEM, P tiles written
+  uint32_t n_q[kRowWarps], n_s_read[kRowWarps], n_p_done[kRowWarps];
   uint64_t xin_full[2][kRowWarps];    // peer warp w's partial scores landed in inbox slot
   uint64_t inbox_free[2][kRowWarps];  // peer warp w has consumed the slot this CTA writes into
   uint64_t drain, drain_o;
@@ -144,6 +147,23 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, co
   bool ok = true;
   if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, p, bs);
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// The same for the row warps' progress counters: every lane < kRowWarps polls
+// one counter until all have reached `target` (bounded like wait_bar).
+__device__ __forceinline__ bool wait_counters(const uint32_t* ctr, uint32_t target, const Params& p, Bars* bs) {
+  const int lane = threadIdx.x & 31;
+  for (long long i = 0;; ++i) {
+    const bool mine = lane >= kRowWarps || static_cast<int32_t>(ld_acquire_u32(ctr + lane) - target) >= 0;
+    if (__all_sync(0xffffffffu, mine)) return true;
+    if (i >= p.wait_limit || *reinterpret_cast<volatile int*>(&bs->abort)) {
+      if (lane == 0) {
+        report(p.status, MLA_ERR_DEVICE_TIMEOUT);
+        atomicExch(&bs->abort, 1);
+      }
+      return false;
+    }
+  }
 }
 
 // Contiguous slice [lo, hi) of the global tile list handled by worker g.
@@ -223,10 +243,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&bs->empty[s], 1);
     }
     for (int s = 0; s < kRopeSlots; ++s) mbar_init(&bs->rope_empty[s], 1);
-    mbar_init(&bs->q_ready, kRowWarps);
     mbar_init(&bs->s_full, 1);
-    mbar_init(&bs->s_free, kRowWarps);
-    mbar_init(&bs->p_ready, kRowWarps);
+    for (int w = 0; w < kRowWarps; ++w) bs->n_q[w] = bs->n_s_read[w] = bs->n_p_done[w] = 0;
     mbar_init(&bs->p_free, 1);
     for (int s = 0; s < 2; ++s)
       for (int w = 0; w < kRowWarps; ++w) {
@@ -307,14 +325,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t n_units = 0;
       bool ok = true;
       while (ok && iter.next(p, g, u)) {
-        ok = wait_bar_warp(&bs->q_ready, n_units & 1, p, bs);
+        ok = wait_counters(bs->n_q, n_units + 1, p, bs);
         ++n_units;
         if (!ok) break;
         tc_fence_after();
         for (int t = u.ta; t < u.tb && ok; ++t, ++k) {
           // S(k) into the single S buffer once the row warps have read S(k-1) out of it
           if (!(ok = wait_bar_warp(&bs->full[k % kStages], (k / kStages) & 1, p, bs))) break;
-          if (k >= 1 && !(ok = wait_bar_warp(&bs->s_free, (k - 1) & 1, p, bs))) break;
+          if (k >= 1 && !(ok = wait_counters(bs->n_s_read, k, p, bs))) break;
           tc_fence_after();
           const uint32_t st = smem_u32(smem + kOffStages + (k % kStages) * kStageBytes);
           const uint32_t rope = smem_u32(smem + kOffRope + (k % kRopeSlots) * kRopeBoxBytes);
@@ -343,7 +361,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       while (ok && iter.next(p, g, u)) {
         for (int t = u.ta; t < u.tb && ok; ++t, ++k) {
           // P(k) is in TMEM (and S(k) done, so the stage has landed)
-          if (!(ok = wait_bar_warp(&bs->p_ready, k & 1, p, bs))) break;
+          if (!(ok = wait_counters(bs->n_p_done, k + 1, p, bs))) break;
           tc_fence_after();
           const uint32_t st = smem_u32(smem + kOffStages + (k % kStages) * kStageBytes);
           mma_value_tile_elect<kTile / 16>(tmem + kTmemO, tmem + kTmemP, smem_desc(st, kBoxBytes, 1024, kSwizzle128B),
@@ -378,6 +396,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t n_send = 0;   // partial blocks sent to the peer
     uint32_t n_recv = 0;   // partial blocks received from it
     uint32_t n_p = 0;      // P tiles written (global) = tile index for the stage ring
+    uint32_t n_units_q = 0;  // query tokens loaded
     bool ok = true;
 
     // Reads S out of TMEM and scales it to log2 units (kept in `own`, fp32);
@@ -392,7 +411,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bs->s_free);
+      if (lane == 0) st_release_u32(&bs->n_s_read[warp - 2], n_s);
       uint32_t h[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -445,7 +464,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bs->q_ready);
+        if (lane == 0) st_release_u32(&bs->n_q[warp - 2], n_units_q + 1);
+        ++n_units_q;
       }
       const int n = u.tb - u.ta;
       float2 cur[32], nxt[32];  // key pairs (2j, 2j+1) of the tile being combined / the next tile
@@ -535,12 +555,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int row = valid + (idx >> 5), box = (idx >> 3) & 3, ch = idx & 7;
             *reinterpret_cast<uint4*>(st + box * kBoxBytes + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
           }
-          fence_proxy_async_smem();  // each warp's p_ready arrival covers its own share
+          fence_proxy_async_smem();  // each warp's P counter release covers its own share
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&bs->p_ready);
+          st_release_u32(&bs->n_p_done[warp - 2], n_p + 1);
           mbar_arrive_relaxed_cluster(peer_free0 + rslot * kBarSlot);  // its values are consumed
         }
         ++n_p;

@@ -57,6 +57,17 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
+// Shared-memory counters with release / acquire semantics: a cheaper hand-off
+// than an mbarrier round trip between warps of one CTA (the consumer polls).
+__device__ __forceinline__ void st_release_u32(uint32_t* addr, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(addr)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(addr)) : "memory");
+  return v;
+}
+
 // ------------------------------------------------------------------ programmatic dependent launch
 // Kernels of the library are launched so that the next kernel in the stream
 // may start while this one finishes.  Every kernel waits (pdl_wait) before it
