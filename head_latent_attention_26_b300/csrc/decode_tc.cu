@@ -104,6 +104,8 @@ struct Params {
   const int* seq_lens;
   const int* cu_q;
   const int* prefix;  // [n_tok+1] tiles before each token (workspace)
+  const int2* tok_info;      // [n_tok] (sequence, position) of each query token (workspace)
+  const int* worker_first;   // [workers] first token of each worker's tile range (workspace)
   __nv_bfloat16* o_lat;
   float* lse;
   float* part_o;      // [2W][128][512]
@@ -172,16 +174,6 @@ __device__ __forceinline__ void worker_range(int g, int workers, int total, int&
   hi = static_cast<int>(static_cast<long long>(g + 1) * total / workers);
 }
 
-__device__ __forceinline__ int first_token_at(const int* prefix, int n_tok, int x) {
-  // largest n with prefix[n] <= x (tiles of token n are [prefix[n], prefix[n+1]))
-  int lo = 0, hi = n_tok - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (__ldg(prefix + mid) <= x) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 struct Unit {
   int n;          // query token
   int ta, tb;     // tile range within the token
@@ -190,7 +182,10 @@ struct Unit {
   int slot;       // partial slot, or -1 when the unit covers the whole token
 };
 
-// Iterates the units of a worker; every role walks the same list.
+// Iterates the units of a worker; every role walks the same list.  The plan
+// kernel stored what a unit needs (tile prefix sums, each token's sequence and
+// position, each worker's first token), so a unit costs one round of
+// independent loads instead of chains of dependent searches.
 struct UnitIter {
   int x, hi, n, first;
   __device__ bool next(const Params& p, int g, Unit& u) {
@@ -200,8 +195,9 @@ struct UnitIter {
       u.n = n;
       u.ta = x - t0;
       u.tb = min(hi, t1) - t0;
-      u.b = seq_of_token(p.cu_q, p.batch, n);
-      u.pos = __ldg(p.seq_lens + u.b) - (__ldg(p.cu_q + u.b + 1) - n);
+      const int2 info = __ldg(p.tok_info + n);
+      u.b = info.x;
+      u.pos = info.y;
       const bool complete = (u.ta == 0 && u.tb == t1 - t0);
       u.slot = complete ? -1 : 2 * g + (first ? 0 : 1);
       first = 0;
@@ -217,7 +213,7 @@ __device__ __forceinline__ UnitIter make_iter(const Params& p, int g) {
   const int total = __ldg(p.prefix + p.n_tok);
   UnitIter it;
   worker_range(g, p.workers, total, it.x, it.hi);
-  it.n = it.x < it.hi ? first_token_at(p.prefix, p.n_tok, it.x) : 0;
+  it.n = it.x < it.hi ? __ldg(p.worker_first + g) : 0;
   it.first = 1;
   return it;
 }
@@ -659,30 +655,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-// prefix[n] = tiles of all tokens before n; tiles of token n = pos_n/64 + 1.
+__device__ __forceinline__ int worker_of(long long x, int workers, int total) {
+  int g = static_cast<int>(x * workers / total);
+  while (g + 1 < workers && static_cast<long long>(g + 1) * total / workers <= x) ++g;
+  while (g > 0 && static_cast<long long>(g) * total / workers > x) --g;
+  return g;
+}
+
+constexpr int kPlanSmemSeqs = 4096;  // cu_q entries the plan kernel keeps in shared memory
+
+// The plan of a decode call, from the sequence metadata:
+//   prefix[n]       = tiles of all tokens before n (tiles of token n = pos_n/64 + 1)
+//   tok_info[n]     = (sequence, position) of token n
+//   worker_first[g] = the token holding the first tile of worker g's range
+// One CTA; cu_q sits in shared memory so that finding a token's sequence is a
+// search in shared memory rather than a chain of dependent global loads.
 __global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ seq_lens, const int* __restrict__ cu_q,
-                                                    int batch, int n_tok, int max_blocks, int* __restrict__ prefix,
-                                                    int* status) {
+                                                    int batch, int n_tok, int max_blocks, int workers,
+                                                    int* __restrict__ prefix, int2* __restrict__ tok_info,
+                                                    int* __restrict__ worker_first, int* status) {
   __shared__ int warp_sums[32];
   __shared__ int carry;
+  __shared__ int s_cu[kPlanSmemSeqs + 1];
   if (threadIdx.x == 0) pdl_trigger();  // the decode CTAs may set up meanwhile
   pdl_wait();
+  const bool cu_smem = batch <= kPlanSmemSeqs;
+  if (cu_smem)
+    for (int i = threadIdx.x; i <= batch; i += blockDim.x) s_cu[i] = __ldg(cu_q + i);
   if (threadIdx.x == 0) { carry = 0; prefix[0] = 0; }
   if (threadIdx.x == 0 && __ldg(cu_q + batch) != n_tok) report(status, MLA_ERR_DEVICE_BOUNDS);
   __syncthreads();
+  const int* cu = cu_smem ? s_cu : cu_q;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int base = 0; base < n_tok; base += 1024) {
     const int n = base + threadIdx.x;
     int tiles = 0;
     if (n < n_tok) {
-      const int b = seq_of_token(cu_q, batch, n);
-      const int pos = __ldg(seq_lens + b) - (__ldg(cu_q + b + 1) - n);
-      if (pos < 0 || n < __ldg(cu_q + b) || n >= __ldg(cu_q + b + 1) || pos / kBlockRows >= max_blocks) {
+      const int b = seq_of_token(cu, batch, n);
+      const int c0 = cu[b], c1 = cu[b + 1];
+      const int pos = __ldg(seq_lens + b) - (c1 - n);
+      if (pos < 0 || n < c0 || n >= c1 || pos / kBlockRows >= max_blocks) {
         report(status, MLA_ERR_DEVICE_BOUNDS);
         tiles = pos >= 0 ? min(pos / kTile + 1, max_blocks * (kBlockRows / kTile)) : 0;
       } else {
         tiles = pos / kTile + 1;
       }
+      tok_info[n] = make_int2(b, pos);
     }
     int v = tiles;
 #pragma unroll
@@ -708,13 +726,18 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ seq_
     if (threadIdx.x == 1023) carry = incl;
     __syncthreads();
   }
-}
-
-__device__ __forceinline__ int worker_of(long long x, int workers, int total) {
-  int g = static_cast<int>(x * workers / total);
-  while (g + 1 < workers && static_cast<long long>(g + 1) * total / workers <= x) ++g;
-  while (g > 0 && static_cast<long long>(g) * total / workers > x) --g;
-  return g;
+  // every worker's first tile lo_g = g * total / W lies in exactly one token
+  const int total = carry;
+  if (total <= 0) return;
+  for (int n = threadIdx.x; n < n_tok; n += blockDim.x) {
+    const int t0 = prefix[n], t1 = prefix[n + 1];  // written above by this CTA
+    if (t1 <= t0) continue;
+    for (int g = worker_of(t0, workers, total); g < workers; ++g) {
+      const long long lo = static_cast<long long>(g) * total / workers;
+      if (lo >= t1) break;
+      if (lo >= t0) worker_first[g] = n;
+    }
+  }
 }
 
 // Merge the pieces of every token whose keys were split across workers:
@@ -813,8 +836,9 @@ bool encode_pool_map(CUtensorMap* m, const void* pool, long long rows, uint32_t 
 // plan -> decode -> combine, each allowed to launch while its predecessor finishes.
 cudaError_t launch_decode_kernels(const Maps& maps, const Params& prm, int W, int n_tok, const int* seq_lens,
                                   const int* cu_q, int batch, int max_blocks, float* lse, int* status, cudaStream_t s) {
-  cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s, 1, seq_lens, cu_q, batch, n_tok, max_blocks,
-                             const_cast<int*>(prm.prefix), status);
+  cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s, 1, seq_lens, cu_q, batch, n_tok, max_blocks, W,
+                             const_cast<int*>(prm.prefix), const_cast<int2*>(prm.tok_info),
+                             const_cast<int*>(prm.worker_first), status);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -829,14 +853,36 @@ int resolve_workers(const mla_handle* h, int num_workers) {
   return num_workers > 0 ? num_workers : max(1, h->num_sms / 2);
 }
 
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Byte offsets of the decode workspace: plan (prefix sums, token info, worker
+// first tokens), then the split-KV partial outputs and their log-sum-exps.
+struct WsLayout {
+  size_t prefix, tok_info, worker_first, part_o, part_lse, total;
+};
+constexpr WsLayout ws_layout(size_t n_tok, size_t W) {
+  WsLayout l{};
+  l.prefix = 0;
+  l.tok_info = l.prefix + align256(sizeof(int) * (n_tok + 1));
+  l.worker_first = l.tok_info + align256(sizeof(int2) * n_tok);
+  l.part_o = l.worker_first + align256(sizeof(int) * W);
+  l.part_lse = l.part_o + align256(sizeof(float) * 2 * W * kHeads * kDc);
+  l.total = l.part_lse + align256(sizeof(float) * 2 * W * kHeads);
+  return l;
+}
+
+void set_workspace(Params& prm, uint8_t* w, const WsLayout& l) {
+  prm.prefix = reinterpret_cast<const int*>(w + l.prefix);
+  prm.tok_info = reinterpret_cast<const int2*>(w + l.tok_info);
+  prm.worker_first = reinterpret_cast<const int*>(w + l.worker_first);
+  prm.part_o = reinterpret_cast<float*>(w + l.part_o);
+  prm.part_lse = reinterpret_cast<float*>(w + l.part_lse);
+}
 
 }  // namespace
 
 size_t decode_tc_workspace_bytes(const mla_handle* h, int n_tok, int num_workers) {
-  const size_t W = static_cast<size_t>(resolve_workers(h, num_workers));
-  return align256(sizeof(int) * (static_cast<size_t>(n_tok) + 1)) + align256(sizeof(float) * 2 * W * kHeads * kDc) +
-         align256(sizeof(float) * 2 * W * kHeads);
+  return ws_layout(static_cast<size_t>(n_tok), static_cast<size_t>(resolve_workers(h, num_workers))).total;
 }
 
 cudaError_t launch_decode_tc(const mla_handle* h, const void* q_lat, const void* pool, int n_pool_blocks,
@@ -849,13 +895,8 @@ cudaError_t launch_decode_tc(const mla_handle* h, const void* q_lat, const void*
   if (!encode_pool_map(&maps.latent, pool, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_pool_map(&maps.rope, pool, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  uint8_t* w = static_cast<uint8_t*>(ws);
   Params prm;
-  prm.prefix = reinterpret_cast<int*>(w);
-  w += align256(sizeof(int) * (static_cast<size_t>(n_tok) + 1));
-  prm.part_o = reinterpret_cast<float*>(w);
-  w += align256(sizeof(float) * 2 * static_cast<size_t>(W) * kHeads * kDc);
-  prm.part_lse = reinterpret_cast<float*>(w);
+  set_workspace(prm, static_cast<uint8_t*>(ws), ws_layout(static_cast<size_t>(n_tok), static_cast<size_t>(W)));
   prm.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
   prm.block_table = block_table;
   prm.seq_lens = seq_lens;
@@ -918,10 +959,8 @@ namespace mla {
 namespace {
 constexpr int kNoAllocMaxTokens = 8192;
 constexpr int kNoAllocMaxWorkers = 32;
-constexpr size_t kNoAllocPrefixBytes = (sizeof(int) * (kNoAllocMaxTokens + 1) + 255) & ~static_cast<size_t>(255);
-constexpr size_t kNoAllocPartOBytes = sizeof(float) * 2 * kNoAllocMaxWorkers * kHeads * kDc;
-constexpr size_t kNoAllocPartLseBytes = sizeof(float) * 2 * kNoAllocMaxWorkers * kHeads;
-constexpr size_t kNoAllocScratchBytes = kNoAllocPrefixBytes + kNoAllocPartOBytes + kNoAllocPartLseBytes;
+constexpr WsLayout kNoAllocLayout = ws_layout(kNoAllocMaxTokens, kNoAllocMaxWorkers);
+constexpr size_t kNoAllocScratchBytes = kNoAllocLayout.total;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -953,11 +992,8 @@ int launch_decode_tc_noalloc(const mla_handle* h, const void* q_lat, const void*
   if (!encode_pool_map(&maps.latent, pool, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_pool_map(&maps.rope, pool, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return 2;
-  uint8_t* w = static_cast<uint8_t*>(g_noalloc_ptr[dev]);
   Params prm;
-  prm.prefix = reinterpret_cast<int*>(w);
-  prm.part_o = reinterpret_cast<float*>(w + kNoAllocPrefixBytes);
-  prm.part_lse = reinterpret_cast<float*>(w + kNoAllocPrefixBytes + kNoAllocPartOBytes);
+  set_workspace(prm, static_cast<uint8_t*>(g_noalloc_ptr[dev]), kNoAllocLayout);
   prm.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
   prm.block_table = block_table;
   prm.seq_lens = seq_lens;
