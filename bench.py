@@ -36,8 +36,8 @@ METRIC = "MLA decode tokens/s and latent-cache GB/s (% of HBM/tensor roofline), 
 # DRAM bytes (read + write) of one decode_tc_kernel launch on this workload,
 # from the ncu capture summarised in profiles/decode_tc_kernel_b64_t4096.md;
 # valid only while the kernel sources hash to the captured ones.
-PROFILED_DECODE = {"sources": {"decode_tc.cu": "22d1b83bcbab2c49", "ptx.cuh": "eac842c0728bf196"},
-                   "workload": (64, 4096), "traffic_bytes": 327054336}
+PROFILED_DECODE = {"sources": {"decode_tc.cu": "f72d086fc7f562ea", "ptx.cuh": "4ad1c9e099fecea1"},
+                   "workload": (64, 4096), "traffic_bytes": 316270848}
 
 
 def _profiled_traffic(B: int, T: int):
