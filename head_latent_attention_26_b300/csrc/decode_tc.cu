@@ -88,8 +88,9 @@ constexpr uint32_t kSmemBytes = kOffBars + 512 + 1024;      // + alignment slack
 // TMEM columns (512 allocated): O half | Q~ latent half | Q~ RoPE half | P | S
 // (bf16 operands hold two elements per 32-bit column)
 constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemQR = 384, kTmemP = 416, kTmemS = 448;
-constexpr int kThreads = 64 + 32 * kRowWarps + 32;
+constexpr int kThreads = 64 + 32 * kRowWarps + 64;
 constexpr int kValueWarp = 2 + kRowWarps;
+constexpr int kXchgWarp = 3 + kRowWarps;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -122,6 +123,9 @@ struct Bars {
   // progress counters of the row warps, polled by the MMA issuers: query
   // tokens loaded into TMEM, S tiles read out of TMEM, P tiles written
   uint32_t n_q[kRowWarps], n_s_read[kRowWarps], n_p_done[kRowWarps];
+  // outbox hand-off between row warp q and the exchange warp: blocks written,
+  // blocks whose copy to the peer has finished reading the outbox
+  uint32_t n_out_ready[kRowWarps], n_out_free[kRowWarps];
   uint64_t xin_full[2][kRowWarps];    // peer warp w's partial scores landed in inbox slot
   uint64_t inbox_free[2][kRowWarps];  // peer warp w has consumed the slot this CTA writes into
   uint64_t drain, drain_o;
@@ -163,6 +167,18 @@ __device__ __forceinline__ bool wait_counters(const uint32_t* ctr, uint32_t targ
         report(p.status, MLA_ERR_DEVICE_TIMEOUT);
         atomicExch(&bs->abort, 1);
       }
+      return false;
+    }
+  }
+}
+
+// All lanes of a warp poll one counter until it reaches `target` (bounded).
+__device__ __forceinline__ bool wait_counter(const uint32_t* ctr, uint32_t target, const Params& p, Bars* bs) {
+  for (long long i = 0;; ++i) {
+    if (static_cast<int32_t>(ld_acquire_u32(ctr) - target) >= 0) return true;
+    if (i >= p.wait_limit || *reinterpret_cast<volatile int*>(&bs->abort)) {
+      report(p.status, MLA_ERR_DEVICE_TIMEOUT);
+      atomicExch(&bs->abort, 1);
       return false;
     }
   }
@@ -240,7 +256,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kRopeSlots; ++s) mbar_init(&bs->rope_empty[s], 1);
     mbar_init(&bs->s_full, 1);
-    for (int w = 0; w < kRowWarps; ++w) bs->n_q[w] = bs->n_s_read[w] = bs->n_p_done[w] = 0;
+    for (int w = 0; w < kRowWarps; ++w)
+      bs->n_q[w] = bs->n_s_read[w] = bs->n_p_done[w] = bs->n_out_ready[w] = bs->n_out_free[w] = 0;
     mbar_init(&bs->p_free, 1);
     for (int s = 0; s < 2; ++s)
       for (int w = 0; w < kRowWarps; ++w) {
@@ -372,7 +389,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else {
+  } else if (warp < 2 + kRowWarps) {
     // ------------------------------------------------------------ row warps
     const int q = warp & 3;                // TMEM lane quadrant of this warp
     const int r = q * 32 + lane;           // head = TMEM lane
@@ -382,8 +399,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // at the same offset in the peer; row = lane (128 B), 16-byte chunks XOR-swizzled
     const uint8_t* const inbox0 = smem + kOffInbox + q * kXBlockBytes;
     uint8_t* const outbox = smem + kOffOutbox + q * kXBlockBytes;
-    const uint32_t peer_inbox0 = map_to_rank(smem_u32(inbox0), peer);
-    const uint32_t peer_xin0 = map_to_rank(smem_u32(&bs->xin_full[0][q]), peer);
     const uint32_t peer_free0 = map_to_rank(smem_u32(&bs->inbox_free[0][q]), peer);
     const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
     UnitIter iter = make_iter(p, g);
@@ -414,25 +429,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         own[j] = mul_f32x2(make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), scale2);
         h[j] = pack_half2(own[j].x, own[j].y);
       }
-      const uint32_t slot = n_send & 1;
-      if (lane == 0) bulk_wait_read<0>();  // the previous copy has read the outbox
-      __syncwarp();
+      // the exchange warp's copy of the previous block has read the outbox
+      if (n_send >= 1 && !wait_counter(&bs->n_out_free[q], n_send, p, bs)) return false;
       uint8_t* row = outbox + lane * 128;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch)
         *reinterpret_cast<uint4*>(row + ((ch ^ (lane & 7)) * 16)) = make_uint4(h[4 * ch], h[4 * ch + 1], h[4 * ch + 2], h[4 * ch + 3]);
       fence_proxy_async_smem();
       __syncwarp();
-      bool good = true;
-      if (lane == 0) {
-        if (n_send >= 2) good = wait_bar(&bs->inbox_free[slot][q], ((n_send >> 1) - 1) & 1, p, bs, true);
-        if (good) {
-          bulk_copy_to_peer(peer_inbox0 + slot * kXSlotBytes, outbox, kXBlockBytes, peer_xin0 + slot * kBarSlot);
-          bulk_commit();
-        }
-      }
+      if (lane == 0) st_release_u32(&bs->n_out_ready[q], n_send + 1);  // the exchange warp ships it
       ++n_send;
-      return __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+      return true;
     };
 
     while (ok && iter.next(p, g, u)) {
@@ -573,8 +580,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // this warp's (idle) outbox block so that every global store instruction
       // covers whole row segments of 4 heads (fp32) or 8 heads (bf16) instead
       // of 32 scattered 16-byte pieces.
-      if (lane == 0) bulk_wait_read<0>();  // no copy still reads the outbox
-      __syncwarp();
+      if (!(ok = wait_counter(&bs->n_out_free[q], n_send, p, bs))) break;  // no copy still reads the outbox
       uint8_t* const stg = outbox;         // 32 rows x 128 B
       const size_t row0 = static_cast<size_t>(u.slot < 0 ? u.n : u.slot) * kHeads + q * 32;  // first head of the warp
       if (u.slot < 0) {
@@ -638,11 +644,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
     }
+  } else if (warp == kXchgWarp) {
+    // ------------------------------------------------------------ exchange issuer
+    // Lane q ships row warp q's fp16 partial block of every tile to the same
+    // warp's inbox in the peer: once the block is written, and once the peer
+    // has consumed what it received into that inbox slot two tiles ago.  This
+    // keeps the copy issue and its waits off the softmax warps' chain.
+    const int q = lane & (kRowWarps - 1);
+    const uint8_t* const outbox_q = smem + kOffOutbox + q * kXBlockBytes;
+    const uint32_t peer_inbox_q = map_to_rank(smem_u32(smem + kOffInbox + q * kXBlockBytes), peer);
+    const uint32_t peer_xin_q = map_to_rank(smem_u32(&bs->xin_full[0][q]), peer);
+    UnitIter iter = make_iter(p, g);
+    Unit u;
+    uint32_t i = 0;  // blocks shipped per row warp
+    bool ok = true;
+    while (ok && iter.next(p, g, u)) {
+      for (int t = u.ta; t < u.tb && ok; ++t, ++i) {
+        if (!(ok = wait_counters(bs->n_out_ready, i + 1, p, bs))) break;
+        const uint32_t slot = i & 1;
+        bool good = true;
+        if (lane < kRowWarps) {
+          if (i >= 2) good = wait_bar(&bs->inbox_free[slot][q], ((i >> 1) - 1) & 1, p, bs, true);
+          if (good) {
+            bulk_copy_to_peer(peer_inbox_q + slot * kXSlotBytes, outbox_q, kXBlockBytes, peer_xin_q + slot * kBarSlot);
+            bulk_commit();
+            bulk_wait_read<0>();
+            st_release_u32(&bs->n_out_free[q], i + 1);
+          }
+        }
+        ok = __all_sync(0xffffffffu, good);
+      }
+    }
     // a copy into the peer must not outlive the peer: wait until the peer has
-    // consumed everything this warp sent (its inbox_free arrivals)
-    if (lane == 0) bulk_wait_all();
-    for (uint32_t k = (n_send > 2 ? n_send - 2 : 0); ok && k < n_send; ++k)
-      ok = wait_bar(&bs->inbox_free[k & 1][q], (k >> 1) & 1, p, bs, true);
+    // consumed everything shipped (its inbox_free arrivals)
+    if (lane < kRowWarps) {
+      bulk_wait_all();
+      for (uint32_t k = (i > 2 ? i - 2 : 0); ok && k < i; ++k)
+        ok = wait_bar(&bs->inbox_free[k & 1][q], (k >> 1) & 1, p, bs, true);
+    }
   }
 
   __syncthreads();
