@@ -106,7 +106,8 @@ struct Params {
   const int* cu_q;
   const int* prefix;  // [n_tok+1] tiles before each token (workspace)
   const int2* tok_info;      // [n_tok] (sequence, position) of each query token (workspace)
-  const int* worker_first;   // [workers] first token of each worker's tile range (workspace)
+  const int* worker_plan;    // [workers][4] tile range [lo, hi) and first token of each worker (workspace)
+  const int* plan_flags;     // [1] 1 when worker ranges split tokens (workspace)
   __nv_bfloat16* o_lat;
   float* lse;
   float* part_o;      // [2W][128][512]
@@ -226,10 +227,11 @@ struct UnitIter {
 };
 
 __device__ __forceinline__ UnitIter make_iter(const Params& p, int g) {
-  const int total = __ldg(p.prefix + p.n_tok);
   UnitIter it;
-  worker_range(g, p.workers, total, it.x, it.hi);
-  it.n = it.x < it.hi ? __ldg(p.worker_first + g) : 0;
+  const int4 wp = __ldg(reinterpret_cast<const int4*>(p.worker_plan) + g);
+  it.x = wp.x;
+  it.hi = wp.y;
+  it.n = it.x < it.hi ? wp.z : 0;
   it.first = 1;
   return it;
 }
@@ -702,26 +704,36 @@ __device__ __forceinline__ int worker_of(long long x, int workers, int total) {
 }
 
 constexpr int kPlanSmemSeqs = 4096;  // cu_q entries the plan kernel keeps in shared memory
+// Whole tokens per worker when the longest token has at most this many tiles
+// more than an even share: splitting costs each split worker a partial write
+// and the call a combine pass, about that many tiles of work.
+constexpr int kWholeTokenSlack = 12;
 
 // The plan of a decode call, from the sequence metadata:
-//   prefix[n]       = tiles of all tokens before n (tiles of token n = pos_n/64 + 1)
-//   tok_info[n]     = (sequence, position) of token n
-//   worker_first[g] = the token holding the first tile of worker g's range
-// One CTA; cu_q sits in shared memory so that finding a token's sequence is a
-// search in shared memory rather than a chain of dependent global loads.
+//   prefix[n]         = tiles of all tokens before n (tiles of token n = pos_n/64 + 1)
+//   tok_info[n]       = (sequence, position) of token n
+//   worker_plan[g]    = (lo, hi, first token, 0): worker g's range [lo, hi) of
+//                       the global tile list and the token holding tile lo
+//   plan_flags[0]     = 1 when ranges split tokens (the combine kernel merges)
+// Two layouts: with no more tokens than workers and tokens of similar length,
+// worker g takes token g whole (nothing to merge); otherwise the tile list is
+// cut into W balanced contiguous ranges.  One CTA; cu_q sits in shared memory
+// so that finding a token's sequence is a search in shared memory rather than
+// a chain of dependent global loads.
 __global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ seq_lens, const int* __restrict__ cu_q,
                                                     int batch, int n_tok, int max_blocks, int workers,
                                                     int* __restrict__ prefix, int2* __restrict__ tok_info,
-                                                    int* __restrict__ worker_first, int* status) {
+                                                    int* __restrict__ worker_plan, int* __restrict__ plan_flags,
+                                                    int* status) {
   __shared__ int warp_sums[32];
-  __shared__ int carry;
+  __shared__ int carry, max_tiles;
   __shared__ int s_cu[kPlanSmemSeqs + 1];
   if (threadIdx.x == 0) pdl_trigger();  // the decode CTAs may set up meanwhile
   pdl_wait();
   const bool cu_smem = batch <= kPlanSmemSeqs;
   if (cu_smem)
     for (int i = threadIdx.x; i <= batch; i += blockDim.x) s_cu[i] = __ldg(cu_q + i);
-  if (threadIdx.x == 0) { carry = 0; prefix[0] = 0; }
+  if (threadIdx.x == 0) { carry = 0; max_tiles = 0; prefix[0] = 0; }
   if (threadIdx.x == 0 && __ldg(cu_q + batch) != n_tok) report(status, MLA_ERR_DEVICE_BOUNDS);
   __syncthreads();
   const int* cu = cu_smem ? s_cu : cu_q;
@@ -740,6 +752,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ seq_
         tiles = pos / kTile + 1;
       }
       tok_info[n] = make_int2(b, pos);
+      atomicMax(&max_tiles, tiles);
     }
     int v = tiles;
 #pragma unroll
@@ -765,16 +778,32 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ seq_
     if (threadIdx.x == 1023) carry = incl;
     __syncthreads();
   }
-  // every worker's first tile lo_g = g * total / W lies in exactly one token
   const int total = carry;
-  if (total <= 0) return;
+  const bool whole = n_tok <= workers && max_tiles <= (total + workers - 1) / workers + kWholeTokenSlack;
+  if (threadIdx.x == 0) plan_flags[0] = whole ? 0 : 1;
+  for (int g = threadIdx.x; g < workers; g += blockDim.x) {
+    int lo, hi;
+    if (whole) {
+      lo = g < n_tok ? prefix[g] : total;  // prefix written above by this CTA
+      hi = g < n_tok ? prefix[g + 1] : total;
+    } else {
+      worker_range(g, workers, total, lo, hi);
+    }
+    worker_plan[4 * g] = lo;
+    worker_plan[4 * g + 1] = hi;
+    worker_plan[4 * g + 2] = whole && g < n_tok ? g : 0;
+    worker_plan[4 * g + 3] = 0;
+  }
+  if (whole || total <= 0) return;
+  __syncthreads();
+  // balanced ranges: every worker's first tile g * total / W lies in exactly one token
   for (int n = threadIdx.x; n < n_tok; n += blockDim.x) {
-    const int t0 = prefix[n], t1 = prefix[n + 1];  // written above by this CTA
+    const int t0 = prefix[n], t1 = prefix[n + 1];
     if (t1 <= t0) continue;
     for (int g = worker_of(t0, workers, total); g < workers; ++g) {
       const long long lo = static_cast<long long>(g) * total / workers;
       if (lo >= t1) break;
-      if (lo >= t0) worker_first[g] = n;
+      if (lo >= t0) worker_plan[4 * g + 2] = n;
     }
   }
 }
@@ -785,12 +814,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ seq_
 // One warp per (token, head); the pieces of a token are the workers g0..g1
 // whose ranges meet its tiles.  Worker g wrote slot 2g when its range starts
 // inside the token, else 2g+1 (its range started in an earlier token).
-__global__ void __launch_bounds__(256) combine_kernel(const int* __restrict__ prefix, int n_tok, int workers,
-                                                      const float* __restrict__ part_o,
+__global__ void __launch_bounds__(256) combine_kernel(const int* __restrict__ prefix, const int* __restrict__ plan_flags,
+                                                      int n_tok, int workers, const float* __restrict__ part_o,
                                                       const float* __restrict__ part_lse,
                                                       __nv_bfloat16* __restrict__ o_lat, float* __restrict__ lse) {
   if (threadIdx.x == 0) pdl_trigger();
   pdl_wait();
+  if (__ldg(plan_flags) == 0) return;  // whole tokens per worker: nothing was split
   const int n = blockIdx.x;
   const int total = __ldg(prefix + n_tok);
   const int t0 = __ldg(prefix + n), t1 = __ldg(prefix + n + 1);
@@ -877,14 +907,14 @@ cudaError_t launch_decode_kernels(const Maps& maps, const Params& prm, int W, in
                                   const int* cu_q, int batch, int max_blocks, float* lse, int* status, cudaStream_t s) {
   cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s, 1, seq_lens, cu_q, batch, n_tok, max_blocks, W,
                              const_cast<int*>(prm.prefix), const_cast<int2*>(prm.tok_info),
-                             const_cast<int*>(prm.worker_first), status);
+                             const_cast<int*>(prm.worker_plan), const_cast<int*>(prm.plan_flags), status);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   e = launch_pdl(decode_tc_kernel, dim3(2 * W), dim3(kThreads), kSmemBytes, s, 1, maps, prm);
   if (e != cudaSuccess) return e;
   return launch_pdl(combine_kernel, dim3(n_tok, kHeads / 8), dim3(256), 0, s, 1, static_cast<const int*>(prm.prefix),
-                    n_tok, W, static_cast<const float*>(prm.part_o), static_cast<const float*>(prm.part_lse), prm.o_lat,
+                    prm.plan_flags, n_tok, W, static_cast<const float*>(prm.part_o), static_cast<const float*>(prm.part_lse), prm.o_lat,
                     lse);
 }
 
@@ -895,16 +925,18 @@ int resolve_workers(const mla_handle* h, int num_workers) {
 constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Byte offsets of the decode workspace: plan (prefix sums, token info, worker
-// first tokens), then the split-KV partial outputs and their log-sum-exps.
+// ranges, layout flag), then the split-KV partial outputs and their
+// log-sum-exps.
 struct WsLayout {
-  size_t prefix, tok_info, worker_first, part_o, part_lse, total;
+  size_t prefix, tok_info, worker_plan, plan_flags, part_o, part_lse, total;
 };
 constexpr WsLayout ws_layout(size_t n_tok, size_t W) {
   WsLayout l{};
   l.prefix = 0;
   l.tok_info = l.prefix + align256(sizeof(int) * (n_tok + 1));
-  l.worker_first = l.tok_info + align256(sizeof(int2) * n_tok);
-  l.part_o = l.worker_first + align256(sizeof(int) * W);
+  l.worker_plan = l.tok_info + align256(sizeof(int2) * n_tok);
+  l.plan_flags = l.worker_plan + align256(sizeof(int4) * W);
+  l.part_o = l.plan_flags + 256;
   l.part_lse = l.part_o + align256(sizeof(float) * 2 * W * kHeads * kDc);
   l.total = l.part_lse + align256(sizeof(float) * 2 * W * kHeads);
   return l;
@@ -913,7 +945,8 @@ constexpr WsLayout ws_layout(size_t n_tok, size_t W) {
 void set_workspace(Params& prm, uint8_t* w, const WsLayout& l) {
   prm.prefix = reinterpret_cast<const int*>(w + l.prefix);
   prm.tok_info = reinterpret_cast<const int2*>(w + l.tok_info);
-  prm.worker_first = reinterpret_cast<const int*>(w + l.worker_first);
+  prm.worker_plan = reinterpret_cast<const int*>(w + l.worker_plan);
+  prm.plan_flags = reinterpret_cast<const int*>(w + l.plan_flags);
   prm.part_o = reinterpret_cast<float*>(w + l.part_o);
   prm.part_lse = reinterpret_cast<float*>(w + l.part_lse);
 }

@@ -165,7 +165,7 @@ mla_status mla_decode(mla_handle* h, const void* q_lat, const void* pool, int n_
  * it no allocator, or a latency-critical loop that must not call cudaMalloc
  * because that call can synchronise the device and take unbounded time.
  *
- * Its split-KV scratch is one fixed array in device memory (16,908,800 bytes
+ * Its split-KV scratch is one fixed array in device memory (16,909,312 bytes
  * on the tensor path), created when the library is loaded and kept by every
  * device that loads it until the process exits.  Limits: n_tok <= 8192 and
  * at most 32 workers (num_workers = 0 picks min(SMs/2, 32)); larger requests
