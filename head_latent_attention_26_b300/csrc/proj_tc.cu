@@ -46,6 +46,7 @@ constexpr int kBK = 64;                        // k per stage (one 128-byte swiz
 constexpr uint32_t kABytes = kBM * kBK * 2;    // 16 KB weight tile
 constexpr int kThreads = 128;
 constexpr int kMaxSplit = 16;                  // cluster size (above 8 needs the non-portable opt-in)
+constexpr int kMaxDevices = 16;                // devices whose resident-cluster counts are cached
 
 enum : int { kModeLinear = 0, kModeAppend = 1, kModeAbsorb = 2 };
 
@@ -406,6 +407,37 @@ cudaError_t launch_proj_nt(const ProjMaps& maps, const ProjParams& p, int nsplit
   if (nsplit > 8) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
+  }
+  // The largest split (cluster size) not above nsplit whose clusters can all
+  // be resident at once: clusters are placed within one GPC, so a split that
+  // fits the SM count can still leave a second wave.  Per device and cluster
+  // size, the resident-cluster count is asked once and kept.
+  static int resident[kMaxDevices][kMaxSplit + 1];
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = -1;
+  const int clusters = tile_groups * n_tiles;
+  for (; nsplit > 1; --nsplit) {
+    int ncl = dev >= 0 ? resident[dev][nsplit] : 0;
+    if (ncl == 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(nsplit, tile_groups, n_tiles);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = kSmem;
+      cudaLaunchAttribute a[1];
+      a[0].id = cudaLaunchAttributeClusterDimension;
+      a[0].val.clusterDim.x = nsplit;
+      a[0].val.clusterDim.y = 1;
+      a[0].val.clusterDim.z = 1;
+      cfg.attrs = a;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();  // not fatal: fall back to the SM-count estimate
+        break;
+      }
+      if (ncl <= 0) ncl = -1;
+      if (dev >= 0) resident[dev][nsplit] = ncl;
+    }
+    if (ncl >= clusters) break;
   }
   return launch_pdl(kern, dim3(nsplit, tile_groups, n_tiles), dim3(kThreads, 1, 1), kSmem, s, nsplit, maps, p);
 }
