@@ -76,21 +76,22 @@ constexpr int kRopeSlots = 3;          // RoPE boxes live only until their score
 constexpr uint32_t kBoxBytes = kTile * 128;                 // 64 keys x 64 cols bf16 (128B swizzle)
 constexpr uint32_t kRopeBoxBytes = kTile * 64;              // 64 keys x 32 cols bf16 (64B swizzle)
 constexpr uint32_t kStageBytes = 4 * kBoxBytes;             // 32768: the latent columns of a tile
-constexpr int kRowWarps = 4;
-constexpr uint32_t kXBlockBytes = 32 * kTile * 2;           // one warp's 32 heads x 64 keys fp16
+constexpr int kRowWarps = 8;                                // softmax warps: 16 heads each
+constexpr uint32_t kXBlockBytes = 16 * kTile * 2;           // one warp's 16 heads x 64 keys fp16
 constexpr uint32_t kXSlotBytes = kRowWarps * kXBlockBytes;  // all row warps
 constexpr uint32_t kOffStages = 0;
 constexpr uint32_t kOffRope = kOffStages + kStages * kStageBytes;
 constexpr uint32_t kOffInbox = kOffRope + kRopeSlots * kRopeBoxBytes;
 constexpr uint32_t kOffOutbox = kOffInbox + 2 * kXSlotBytes;  // one slot: a copy reads it long before reuse
 constexpr uint32_t kOffBars = kOffOutbox + kXSlotBytes;
-constexpr uint32_t kSmemBytes = kOffBars + 512 + 1024;      // + alignment slack
+constexpr uint32_t kSmemBytes = kOffBars + 1024 + 1024;     // + alignment slack
 // TMEM columns (512 allocated): O half | Q~ latent half | Q~ RoPE half | P | S
 // (bf16 operands hold two elements per 32-bit column)
 constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemQR = 384, kTmemP = 416, kTmemS = 448;
-constexpr int kThreads = 64 + 32 * kRowWarps + 64;
-constexpr int kValueWarp = 2 + kRowWarps;
-constexpr int kXchgWarp = 3 + kRowWarps;
+constexpr int kValueWarp = 2;                  // value-MMA issuer
+constexpr int kXchgWarp = 3;                   // ships the softmax warps' partial blocks to the peer
+constexpr int kFirstRowWarp = 4;               // softmax warps 4 .. 4 + kRowWarps - 1
+constexpr int kThreads = 32 * (kFirstRowWarp + kRowWarps);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -133,8 +134,8 @@ struct Bars {
   uint32_t tmem_base;
   int abort;
 };
-static_assert(sizeof(Bars) <= 512, "barrier block");
-constexpr uint32_t kBarSlot = kRowWarps * sizeof(uint64_t);  // stride of one slot in the [2][8] barrier arrays
+static_assert(sizeof(Bars) <= 1024, "barrier block");
+constexpr uint32_t kBarSlot = kRowWarps * sizeof(uint64_t);  // stride of one slot of xin_full / inbox_free
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Params& p, Bars* bs,
                                          bool cluster_scope = false) {
@@ -391,17 +392,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp < 2 + kRowWarps) {
+  } else if (warp >= kFirstRowWarp) {
     // ------------------------------------------------------------ row warps
-    const int q = warp & 3;                // TMEM lane quadrant of this warp
-    const int r = q * 32 + lane;           // head = TMEM lane
-    const int tr = threadIdx.x - 64;       // 0..127 among the row warps
-    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    // this warp's 4 KB block of inbox slot s sits at inbox0 + s * kXSlotBytes,
-    // at the same offset in the peer; row = lane (128 B), 16-byte chunks XOR-swizzled
-    const uint8_t* const inbox0 = smem + kOffInbox + q * kXBlockBytes;
-    uint8_t* const outbox = smem + kOffOutbox + q * kXBlockBytes;
-    const uint32_t peer_free0 = map_to_rank(smem_u32(&bs->inbox_free[0][q]), peer);
+    // Softmax warp rw owns 16 heads: TMEM lanes 32q + 16hh .. +16 of its
+    // quadrant q, read and written with the 16-lane shapes.  Thread t holds
+    // heads ha = 32q + 16hh + t/4 and ha + 8 and, of every 64-key tile, the
+    // key pairs 4j + t%4 (keys 8j + 2(t%4), +1; j = 0..7): register pair k =
+    // 2j + e is key pair 4j + t%4 of head ha (e = 0) or ha + 8 (e = 1).  The
+    // four threads of a head share its running max through two shuffles.
+    const int rw = warp - kFirstRowWarp;
+    const int q = warp & 3;
+    const int hh = rw >> 2;
+    const int t4 = lane & 3;
+    const int ha = q * 32 + hh * 16 + (lane >> 2);
+    const int tr = threadIdx.x - 32 * kFirstRowWarp;  // 0..255 among the row warps
+    const uint32_t lane16 = static_cast<uint32_t>(q * 32 + hh * 16) << 16;
+    const uint32_t lane32 = static_cast<uint32_t>(q * 32) << 16;
+    // this warp's 2 KB block of inbox slot s sits at inbox0 + s * kXSlotBytes,
+    // at the same offset in the peer; row = thread (64 B), 16-byte chunks XOR-swizzled
+    const uint8_t* const inbox0 = smem + kOffInbox + rw * kXBlockBytes;
+    uint8_t* const outbox = smem + kOffOutbox + rw * kXBlockBytes;
+    const uint32_t peer_free0 = map_to_rank(smem_u32(&bs->inbox_free[0][rw]), peer);
+    const int sw = (lane >> 1) & 3;
     const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
     UnitIter iter = make_iter(p, g);
     Unit u;
@@ -412,41 +424,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t n_units_q = 0;  // query tokens loaded
     bool ok = true;
 
-    // Reads S out of TMEM and scales it to log2 units (kept in `own`, fp32);
-    // ships its fp16 rounding to the peer's inbox with one bulk copy.
+    // Reads this thread's 32 scores of S out of TMEM, scaled to log2 units
+    // (kept in `own`, fp32), and hands their fp16 rounding to the exchange warp.
     auto send = [&](float2* own) -> bool {
       if (!wait_bar(&bs->s_full, n_s & 1, p, bs)) return false;
       ++n_s;
       tc_fence_after();
-      uint32_t v[64];
-      tmem_ld32(tmem + lane_base + kTmemS, v);
-      tmem_ld32(tmem + lane_base + kTmemS + 32, v + 32);
+      uint32_t v[32];
+      tmem_ld_16x256b_x8(tmem + lane16 + kTmemS, v);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) st_release_u32(&bs->n_s_read[warp - 2], n_s);
-      uint32_t h[32];
+      if (lane == 0) st_release_u32(&bs->n_s_read[rw], n_s);
+      uint32_t h[16];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        own[j] = mul_f32x2(make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), scale2);
-        h[j] = pack_half2(own[j].x, own[j].y);
+      for (int k = 0; k < 16; ++k) {
+        own[k] = mul_f32x2(make_float2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), scale2);
+        h[k] = pack_half2(own[k].x, own[k].y);
       }
       // the exchange warp's copy of the previous block has read the outbox
-      if (n_send >= 1 && !wait_counter(&bs->n_out_free[q], n_send, p, bs)) return false;
-      uint8_t* row = outbox + lane * 128;
+      if (n_send >= 1 && !wait_counter(&bs->n_out_free[rw], n_send, p, bs)) return false;
+      uint8_t* row = outbox + lane * 64;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4*>(row + ((ch ^ (lane & 7)) * 16)) = make_uint4(h[4 * ch], h[4 * ch + 1], h[4 * ch + 2], h[4 * ch + 3]);
+      for (int ch = 0; ch < 4; ++ch)
+        *reinterpret_cast<uint4*>(row + ((ch ^ sw) * 16)) = make_uint4(h[4 * ch], h[4 * ch + 1], h[4 * ch + 2], h[4 * ch + 3]);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) st_release_u32(&bs->n_out_ready[q], n_send + 1);  // the exchange warp ships it
+      if (lane == 0) st_release_u32(&bs->n_out_ready[rw], n_send + 1);  // the exchange warp ships it
       ++n_send;
       return true;
     };
 
     while (ok && iter.next(p, g, u)) {
-      // ---- latent query: own 256 latent + 32 RoPE columns of head r -> TMEM
-      {
+      // ---- latent query: the first softmax warp of each quadrant writes its
+      // 32 heads' own 256 latent + 32 RoPE columns (thread = head = TMEM lane)
+      if (hh == 0) {
+        const int r = q * 32 + lane;
         const uint4* src = reinterpret_cast<const uint4*>(p.q_lat + (static_cast<size_t>(u.n) * kHeads + r) * kWidth + 256 * c);
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
@@ -456,7 +469,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint4 w = __ldg(src + ch * 4 + j);
             v[4 * j] = w.x; v[4 * j + 1] = w.y; v[4 * j + 2] = w.z; v[4 * j + 3] = w.w;
           }
-          tmem_st16(tmem + lane_base + kTmemQ + ch * 16, v);
+          tmem_st16(tmem + lane32 + kTmemQ + ch * 16, v);
         }
         const uint4* rsrc = reinterpret_cast<const uint4*>(p.q_lat + (static_cast<size_t>(u.n) * kHeads + r) * kWidth + 512 + 32 * c);
         uint32_t v[16];
@@ -465,30 +478,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint4 w = __ldg(rsrc + j);
           v[4 * j] = w.x; v[4 * j + 1] = w.y; v[4 * j + 2] = w.z; v[4 * j + 3] = w.w;
         }
-        tmem_st16(tmem + lane_base + kTmemQR, v);
+        tmem_st16(tmem + lane32 + kTmemQR, v);
         tmem_st_wait();
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) st_release_u32(&bs->n_q[warp - 2], n_units_q + 1);
-        ++n_units_q;
       }
+      __syncwarp();
+      if (lane == 0) st_release_u32(&bs->n_q[rw], n_units_q + 1);
+      ++n_units_q;
       const int n = u.tb - u.ta;
-      float2 cur[32], nxt[32];  // key pairs (2j, 2j+1) of the tile being combined / the next tile
+      float2 cur[16], nxt[16];  // this thread's key pairs of the tile being combined / the next tile
       if (!(ok = send(cur))) break;
-      float m = -INFINITY, l = 0.f;
+      // running max of heads ha / ha + 8 (the same in the head's four threads)
+      // and this thread's partial row sums
+      float ma = -INFINITY, mb = -INFINITY, la = 0.f, lb = 0.f;
       for (int tt = 0; tt < n && ok; ++tt) {
         const int t = u.ta + tt;
         if (tt + 1 < n && !(ok = send(nxt))) break;
         // ---- 1. s = own + peer partial scores of this tile (log2 units)
         const uint32_t rslot = n_recv & 1;
         {
-          if (!(ok = wait_bar(&bs->xin_full[rslot][q], (n_recv >> 1) & 1, p, bs, true))) break;
+          if (!(ok = wait_bar(&bs->xin_full[rslot][rw], (n_recv >> 1) & 1, p, bs, true))) break;
           ++n_recv;
-          if (lane == 0) mbar_arrive_expect_tx(&bs->xin_full[rslot][q], kXBlockBytes);  // arm the next phase
-          const uint8_t* row = inbox0 + rslot * kXSlotBytes + lane * 128;
+          if (lane == 0) mbar_arrive_expect_tx(&bs->xin_full[rslot][rw], kXBlockBytes);  // arm the next phase
+          const uint8_t* row = inbox0 + rslot * kXSlotBytes + lane * 64;
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const uint4 w = *reinterpret_cast<const uint4*>(row + ((ch ^ (lane & 7)) * 16));
+          for (int ch = 0; ch < 4; ++ch) {
+            const uint4 w = *reinterpret_cast<const uint4*>(row + ((ch ^ sw) * 16));
             cur[4 * ch] = add_f32_f16x2(cur[4 * ch], w.x);
             cur[4 * ch + 1] = add_f32_f16x2(cur[4 * ch + 1], w.y);
             cur[4 * ch + 2] = add_f32_f16x2(cur[4 * ch + 2], w.z);
@@ -499,59 +514,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int valid = min(kTile, u.pos - t * kTile + 1);  // keys of this tile the token sees
         if (valid < kTile) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (2 * j >= valid) cur[j].x = -INFINITY;
-            if (2 * j + 1 >= valid) cur[j].y = -INFINITY;
+          for (int k = 0; k < 16; ++k) {
+            const int key = 8 * (k >> 1) + 2 * t4;
+            if (key >= valid) cur[k].x = -INFINITY;
+            if (key + 1 >= valid) cur[k].y = -INFINITY;
           }
         }
-        // tile max: a tree of 3-input maxima over the 64 scores
-        auto sv = [&](int i) -> float { return (i & 1) ? cur[i >> 1].y : cur[i >> 1].x; };
-        float mx[22];
-#pragma unroll
-        for (int j = 0; j < 21; ++j) mx[j] = max3(sv(3 * j), sv(3 * j + 1), sv(3 * j + 2));
-        mx[21] = sv(63);
-        float my[8];
-#pragma unroll
-        for (int j = 0; j < 7; ++j) my[j] = max3(mx[3 * j], mx[3 * j + 1], mx[3 * j + 2]);
-        my[7] = mx[21];
-        const float mt = max3(max3(my[0], my[1], my[2]), max3(my[3], my[4], my[5]), fmaxf(my[6], my[7]));
-        float m_use = m, f = 1.f;
+        // tile max of each head: this thread's 16 scores, then its three partners
+        float xa = max3(max3(cur[0].x, cur[0].y, cur[2].x), max3(cur[2].y, cur[4].x, cur[4].y),
+                        max3(cur[6].x, cur[6].y, cur[8].x));
+        xa = max3(xa, max3(cur[8].y, cur[10].x, cur[10].y), max3(cur[12].x, cur[12].y, fmaxf(cur[14].x, cur[14].y)));
+        float xb = max3(max3(cur[1].x, cur[1].y, cur[3].x), max3(cur[3].y, cur[5].x, cur[5].y),
+                        max3(cur[7].x, cur[7].y, cur[9].x));
+        xb = max3(xb, max3(cur[9].y, cur[11].x, cur[11].y), max3(cur[13].x, cur[13].y, fmaxf(cur[15].x, cur[15].y)));
+        xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 1));
+        xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, 1));
+        xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 2));
+        xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, 2));
+        float mua = ma, mub = mb, fa = 1.f, fb = 1.f;
         if (tt == 0) {
-          m_use = mt;
-        } else if (mt > m + kRescaleThreshold) {
-          m_use = mt;
-          f = ex2_approx(m - mt);
+          mua = xa;
+          mub = xb;
+        } else {
+          if (xa > ma + kRescaleThreshold) { mua = xa; fa = ex2_approx(ma - xa); }
+          if (xb > mb + kRescaleThreshold) { mub = xb; fb = ex2_approx(mb - xb); }
         }
-        const float2 neg_m = make_float2(-m_use, -m_use);
-        uint32_t pk[32];
-        float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        const float2 nma = make_float2(-mua, -mua), nmb = make_float2(-mub, -mub);
+        uint32_t pk[16];
+        float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float2 x = add_f32x2(cur[j], neg_m);
+        for (int k = 0; k < 16; ++k) {
+          const float2 x = add_f32x2(cur[k], (k & 1) ? nmb : nma);
           const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          rs[j & 3] = add_f32x2(rs[j & 3], e);
-          pk[j] = pack_bf16x2(e.x, e.y);
+          if (k & 1) sb = add_f32x2(sb, e); else sa = add_f32x2(sa, e);
+          pk[k] = pack_bf16x2(e.x, e.y);
         }
-        const float2 rs2 = add_f32x2(add_f32x2(rs[0], rs[1]), add_f32x2(rs[2], rs[3]));
-        const float rowsum = rs2.x + rs2.y;
-        l = (tt == 0) ? rowsum : l * f + rowsum;
-        m = m_use;
-        // ---- 3. the previous O MMA is done (P is free); rescale O if the max moved; write P
+        la = (tt == 0) ? sa.x + sa.y : la * fa + (sa.x + sa.y);
+        lb = (tt == 0) ? sb.x + sb.y : lb * fb + (sb.x + sb.y);
+        ma = mua;
+        mb = mub;
+        // ---- 3. the previous O MMA is done (P is free); rescale O if a max moved; write P
         if (n_p >= 1 && !(ok = wait_bar(&bs->p_free, (n_p - 1) & 1, p, bs))) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, f != 1.f)) {
+        if (__any_sync(0xffffffffu, fa != 1.f || fb != 1.f)) {
 #pragma unroll 1
-          for (int ch = 0; ch < 16; ++ch) {
+          for (int ch = 0; ch < 8; ++ch) {
             uint32_t v[16];
-            tmem_ld16(tmem + lane_base + kTmemO + ch * 16, v);
+            tmem_ld_16x256b_x4(tmem + lane16 + kTmemO + ch * 32, v);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * f);
-            tmem_st16(tmem + lane_base + kTmemO + ch * 16, v);
+            for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * ((j & 2) ? fb : fa));
+            tmem_st_16x256b_x4(tmem + lane16 + kTmemO + ch * 32, v);
           }
         }
-        tmem_st16(tmem + lane_base + kTmemP, pk);
-        tmem_st16(tmem + lane_base + kTmemP + 16, pk + 16);
+        tmem_st_16x128b_x8(tmem + lane16 + kTmemP, pk);
         tmem_st_wait();
         // rows past the token's position may hold anything: zero them for the O MMA
         if (valid < kTile) {
@@ -565,84 +581,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          st_release_u32(&bs->n_p_done[warp - 2], n_p + 1);
+          st_release_u32(&bs->n_p_done[rw], n_p + 1);
           mbar_arrive_relaxed_cluster(peer_free0 + rslot * kBarSlot);  // its values are consumed
         }
         ++n_p;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
+        for (int k = 0; k < 16; ++k) cur[k] = nxt[k];
       }
       if (!ok) break;
-      // ---- epilogue: O / l for this head and this CTA's 256 latent columns
+      // ---- epilogue: O / l for heads ha, ha + 8 and this CTA's 256 latent columns
+      la += __shfl_xor_sync(0xffffffffu, la, 1);
+      lb += __shfl_xor_sync(0xffffffffu, lb, 1);
+      la += __shfl_xor_sync(0xffffffffu, la, 2);
+      lb += __shfl_xor_sync(0xffffffffu, lb, 2);
       if (!(ok = wait_bar(&bs->p_free, (n_p - 1) & 1, p, bs))) break;
       tc_fence_after();
-      const float inv_l = 1.f / l;
-      const float lse_val = (m + log2f(l)) * 0.69314718055994531f;
-      // Rows leave TMEM one head per thread; each 32-column chunk goes through
-      // this warp's (idle) outbox block so that every global store instruction
-      // covers whole row segments of 4 heads (fp32) or 8 heads (bf16) instead
-      // of 32 scattered 16-byte pieces.
-      if (!(ok = wait_counter(&bs->n_out_free[q], n_send, p, bs))) break;  // no copy still reads the outbox
-      uint8_t* const stg = outbox;         // 32 rows x 128 B
-      const size_t row0 = static_cast<size_t>(u.slot < 0 ? u.n : u.slot) * kHeads + q * 32;  // first head of the warp
-      if (u.slot < 0) {
-        __nv_bfloat16* const dst = p.o_lat + row0 * kDc + 256 * c;
+      const float inv_la = 1.f / la, inv_lb = 1.f / lb;
+      // O leaves TMEM in 32-column chunks staged through this warp's (idle)
+      // outbox block (16 rows x 128 B fp32, 8-byte slots XOR-swizzled by row)
+      // so that every global store covers whole row segments.
+      if (!(ok = wait_counter(&bs->n_out_free[rw], n_send, p, bs))) break;  // no copy still reads the outbox
+      uint8_t* const stg = outbox;
+      const int ra = lane >> 2;  // staging rows ra (head ha) and ra + 8 (head ha + 8)
+      const size_t row0 = static_cast<size_t>(u.slot < 0 ? u.n : u.slot) * kHeads + q * 32 + hh * 16;
 #pragma unroll 1
-        for (int ch = 0; ch < 8; ++ch) {
-          uint8_t* const wrow = stg + lane * 64;  // 32 bf16 = 64 B per head
+      for (int ch = 0; ch < 8; ++ch) {
+        uint32_t v[16];
+        tmem_ld_16x256b_x4(tmem + lane16 + kTmemO + ch * 32, v);
+        tmem_ld_wait();
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            uint32_t v[16];
-            tmem_ld16(tmem + lane_base + kTmemO + ch * 32 + hf * 16, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-              const int k = 2 * hf + kk;
-              uint32_t o[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                o[j] = pack_bf16x2(__uint_as_float(v[8 * kk + 2 * j]) * inv_l, __uint_as_float(v[8 * kk + 2 * j + 1]) * inv_l);
-              *reinterpret_cast<uint4*>(wrow + ((k ^ ((lane >> 1) & 3)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-          }
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int row = 8 * i + (lane >> 2), k = lane & 3;
-            const uint4 w = *reinterpret_cast<const uint4*>(stg + row * 64 + ((k ^ ((row >> 1) & 3)) * 16));
-            *reinterpret_cast<uint4*>(dst + static_cast<size_t>(row) * kDc + ch * 32 + k * 8) = w;
-          }
-          __syncwarp();
+        for (int j = 0; j < 4; ++j) {
+          const int e = 4 * j + t4;  // float2 slot of columns 8j + 2 t4, +1
+          *reinterpret_cast<float2*>(stg + ra * 128 + 8 * (e ^ (4 * (ra & 3)))) =
+              make_float2(__uint_as_float(v[4 * j]) * inv_la, __uint_as_float(v[4 * j + 1]) * inv_la);
+          *reinterpret_cast<float2*>(stg + (ra + 8) * 128 + 8 * (e ^ (4 * ((ra + 8) & 3)))) =
+              make_float2(__uint_as_float(v[4 * j + 2]) * inv_lb, __uint_as_float(v[4 * j + 3]) * inv_lb);
         }
-        if (c == 0) p.lse[static_cast<size_t>(u.n) * kHeads + r] = lse_val;
-      } else {
-        float* const dst = p.part_o + row0 * kDc + 256 * c;
-#pragma unroll 1
-        for (int ch = 0; ch < 8; ++ch) {
-          uint8_t* const wrow = stg + lane * 128;  // 32 fp32 = 128 B per head
+        __syncwarp();
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            uint32_t v[16];
-            tmem_ld16(tmem + lane_base + kTmemO + ch * 32 + hf * 16, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const int k = 4 * hf + kk;
-              *reinterpret_cast<float4*>(wrow + ((k ^ (lane & 7)) * 16)) =
-                  make_float4(__uint_as_float(v[4 * kk]) * inv_l, __uint_as_float(v[4 * kk + 1]) * inv_l,
-                              __uint_as_float(v[4 * kk + 2]) * inv_l, __uint_as_float(v[4 * kk + 3]) * inv_l);
-            }
-          }
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int row = 4 * i + (lane >> 3), k = lane & 7;
-            const float4 w = *reinterpret_cast<const float4*>(stg + row * 128 + ((k ^ (row & 7)) * 16));
-            *reinterpret_cast<float4*>(dst + static_cast<size_t>(row) * kDc + ch * 32 + k * 4) = w;
-          }
-          __syncwarp();
+        for (int i = 0; i < 4; ++i) {
+          const int rr = 4 * i + (lane >> 3), cu = lane & 7;  // row, 16-byte unit of 4 columns
+          const float4 w = *reinterpret_cast<const float4*>(stg + rr * 128 + 16 * (cu ^ (2 * (rr & 3))));
+          const size_t off = (row0 + rr) * kDc + 256 * c + ch * 32 + 4 * cu;
+          if (u.slot < 0)
+            *reinterpret_cast<uint2*>(p.o_lat + off) = make_uint2(pack_bf16x2(w.x, w.y), pack_bf16x2(w.z, w.w));
+          else
+            *reinterpret_cast<float4*>(p.part_o + off) = w;
         }
-        if (c == 0) p.part_lse[static_cast<size_t>(u.slot) * kHeads + r] = lse_val;
+        __syncwarp();
+      }
+      if (c == 0 && t4 == 0) {
+        const float lse_a = (ma + log2f(la)) * 0.69314718055994531f, lse_b = (mb + log2f(lb)) * 0.69314718055994531f;
+        float* dst = u.slot < 0 ? p.lse + static_cast<size_t>(u.n) * kHeads : p.part_lse + static_cast<size_t>(u.slot) * kHeads;
+        dst[ha] = lse_a;
+        dst[ha + 8] = lse_b;
       }
       tc_fence_before();
     }
