@@ -443,11 +443,19 @@ cudaError_t launch_proj_nt(const ProjMaps& maps, const ProjParams& p, int nsplit
 }
 
 // Token-tile width: the smallest of 64/128/256 that holds every token, else
-// 256-token tiles.  Stages: enough for ~100-150 KB of loads in flight.
+// 256-token tiles.  Stages: enough for ~100-200 KB of loads in flight per SM.
+// With 64-token tiles, a grid whose unsplit tiles fit the SMs runs one CTA
+// per SM with eight stages (a lone CTA with four stages keeps too little in
+// flight to reach its share of HBM bandwidth); larger grids run two CTAs per
+// SM with four.
 template <int MODE, int MT>
-cudaError_t launch_proj(const ProjMaps& maps, const ProjParams& p, int nsplit, int o_tiles, cudaStream_t s) {
+cudaError_t launch_proj(const ProjMaps& maps, const ProjParams& p, int nsplit, int o_tiles, int num_sms,
+                        cudaStream_t s) {
   const int groups = o_tiles / MT;
-  if (p.n_tok <= 64) return launch_proj_nt<64, 4, MODE, MT>(maps, p, nsplit, groups, 1, s);
+  if (p.n_tok <= 64) {
+    if (groups <= num_sms) return launch_proj_nt<64, 8, MODE, MT>(maps, p, nsplit, groups, 1, s);
+    return launch_proj_nt<64, 4, MODE, MT>(maps, p, nsplit, groups, 1, s);
+  }
   if (p.n_tok <= 128) return launch_proj_nt<128, 4, MODE, MT>(maps, p, nsplit, groups, 1, s);
   return launch_proj_nt<256, 3, MODE, (MT > 2 ? 2 : MT)>(maps, p, nsplit, o_tiles / (MT > 2 ? 2 : MT),
                                                         (p.n_tok + 255) / 256, s);
@@ -528,7 +536,7 @@ cudaError_t launch_linear_tc(const mla_handle* h, const void* X, int x_cols, con
   p.y = static_cast<__nv_bfloat16*>(Y);
   p.ldy = ldy;
   p.seg1_tiles = 1 << 30;
-  return launch_proj<kModeLinear, 1>(maps, p, pick_split(h, o_tiles, n_tok, p.k_blocks), o_tiles, s);
+  return launch_proj<kModeLinear, 1>(maps, p, pick_split(h, o_tiles, n_tok, p.k_blocks), o_tiles, h->num_sms, s);
 }
 
 cudaError_t launch_linear2_tc(const mla_handle* h, const void* X, int in, const void* W1, int out1, void* Y1,
@@ -549,7 +557,7 @@ cudaError_t launch_linear2_tc(const mla_handle* h, const void* X, int in, const 
   p.y2 = static_cast<__nv_bfloat16*>(Y2);
   p.ldy2 = ldy2;
   p.seg1_tiles = t1;
-  return launch_proj<kModeLinear, 1>(maps, p, pick_split(h, t1 + t2, n_tok, p.k_blocks), t1 + t2, s);
+  return launch_proj<kModeLinear, 1>(maps, p, pick_split(h, t1 + t2, n_tok, p.k_blocks), t1 + t2, h->num_sms, s);
 }
 
 cudaError_t launch_cache_append_tc(const mla_handle* h, const void* x, const void* w_dkr, const int* seq_idx,
@@ -574,7 +582,7 @@ cudaError_t launch_cache_append_tc(const mla_handle* h, const void* x, const voi
   p.pool = static_cast<__nv_bfloat16*>(pool);
   maps.w2 = maps.w;
   p.seg1_tiles = 1 << 30;
-  return launch_proj<kModeAppend, 1>(maps, p, pick_split(h, o_tiles, n_new, p.k_blocks), o_tiles, s);
+  return launch_proj<kModeAppend, 1>(maps, p, pick_split(h, o_tiles, n_new, p.k_blocks), o_tiles, h->num_sms, s);
 }
 
 cudaError_t launch_absorb_q_tc(const mla_handle* h, const void* q_c, const void* q_r, const int* pos, int n_tok,
@@ -601,7 +609,7 @@ cudaError_t launch_absorb_q_tc(const mla_handle* h, const void* q_c, const void*
   constexpr int kMT = 4;
   if (per_head % kMT != 0) return cudaErrorInvalidValue;
   // d_h = 128 is two k blocks: no split, so no cluster reduction
-  return launch_proj<kModeAbsorb, kMT>(maps, p, 1, per_head * d.n_h, s);
+  return launch_proj<kModeAbsorb, kMT>(maps, p, 1, per_head * d.n_h, h->num_sms, s);
 }
 
 }  // namespace mla
