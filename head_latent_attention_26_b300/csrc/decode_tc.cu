@@ -720,8 +720,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ seq_
   __shared__ int warp_sums[32];
   __shared__ int carry, max_tiles;
   __shared__ int s_cu[kPlanSmemSeqs + 1];
+  // The plan reads only the caller's sequence metadata, which no kernel of the
+  // library writes, and its outputs are read only by this call's decode and
+  // combine kernels: it runs while the previous kernel finishes and waits for
+  // it only before exiting, so that a kernel waiting on the plan has the
+  // previous kernel's results too.
   if (threadIdx.x == 0) pdl_trigger();  // the decode CTAs may set up meanwhile
-  pdl_wait();
   const bool cu_smem = batch <= kPlanSmemSeqs;
   if (cu_smem)
     for (int i = threadIdx.x; i <= batch; i += blockDim.x) s_cu[i] = __ldg(cu_q + i);
@@ -786,7 +790,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ seq_
     worker_plan[4 * g + 2] = whole && g < n_tok ? g : 0;
     worker_plan[4 * g + 3] = 0;
   }
-  if (whole || total <= 0) return;
+  if (whole || total <= 0) {
+    pdl_wait();
+    return;
+  }
   __syncthreads();
   // balanced ranges: every worker's first tile g * total / W lies in exactly one token
   for (int n = threadIdx.x; n < n_tok; n += blockDim.x) {
@@ -798,6 +805,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ seq_
       if (lo >= t0) worker_plan[4 * g + 2] = n;
     }
   }
+  pdl_wait();
 }
 
 // Merge the pieces of every token whose keys were split across workers:
@@ -810,8 +818,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const int* __restrict__ pr
                                                       int n_tok, int workers, const float* __restrict__ part_o,
                                                       const float* __restrict__ part_lse,
                                                       __nv_bfloat16* __restrict__ o_lat, float* __restrict__ lse) {
-  if (threadIdx.x == 0) pdl_trigger();
   pdl_wait();
+  // The next decode call's plan may overwrite the plan data, so the next
+  // kernel may launch only once every CTA has read all of it: CTAs that stop
+  // here exit (an exit counts as the trigger); the others trigger after the
+  // checks below have consumed every value they read.
   if (__ldg(plan_flags) == 0) return;  // whole tokens per worker: nothing was split
   const int n = blockIdx.x;
   const int total = __ldg(prefix + n_tok);
@@ -819,6 +830,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const int* __restrict__ pr
   if (t1 <= t0) return;
   const int g0 = worker_of(t0, workers, total), g1 = worker_of(t1 - 1, workers, total);
   if (g0 == g1) return;  // whole token inside one worker: already final
+  __syncthreads();
+  if (threadIdx.x == 0) pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * 8 + warp;
   // lane k < npieces holds piece k's slot and lse
