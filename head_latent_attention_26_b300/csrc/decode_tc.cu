@@ -15,14 +15,14 @@
 // * Scores: CTA c computes the partial score over its 288 columns,
 //   S_c = Q~[:, own] . C[:, own]^T  (M=128, N=64, K=288), with its half of the
 //   latent query (latent and RoPE parts) resident in TMEM as the A operand.
-// * Each row warp (32 heads, one TMEM lane quadrant) ships its 32 x 64 block
-//   of partial scores, scaled to log2 units and rounded to fp16, to the same
-//   warp's inbox in the peer CTA with one bulk shared-to-shared copy
-//   (completion counted on the peer's mbarrier, no fence), one tile ahead of
-//   the tile it combines, so the exchange hides behind a tile of work.  The
-//   exchange is bound by the SM-to-SM network (about 16 bytes per clock per
-//   SM on this part; bulk copies beat 16-byte st.async stores by 1.6x), which
-//   is why only fp16 partials travel.  Each
+// * Each softmax ("row") warp owns 16 heads and writes their 16 x 64 block of
+//   partial scores, scaled to log2 units and rounded to fp16, to its outbox;
+//   the exchange warp ships it to the same warp's inbox in the peer CTA with
+//   one bulk shared-to-shared copy (completion counted on the peer's mbarrier,
+//   no fence), one tile ahead of the tile it combines, so the exchange hides
+//   behind a tile of work.  The exchange is bound by the SM-to-SM network
+//   (about 16 bytes per clock per SM on this part; bulk copies beat 16-byte
+//   st.async stores by 1.6x), which is why only fp16 partials travel.  Each
 //   CTA adds the peer's fp16 partial to its own fp32 partial and runs the
 //   online softmax on the result; no softmax state is exchanged.  (The two
 //   CTAs' scores differ by the fp16 rounding of one partial, a few 1e-4 in
@@ -42,14 +42,18 @@
 // * Rescaling of O is lazy: the running max only moves when a tile's max
 //   exceeds it by more than 2^8, which keeps every exp2 argument <= 8 and the
 //   result exact (numerator and denominator share the stale max).
-// * Keys of a token can be split across workers (balanced contiguous ranges of
-//   the global tile list); split pieces write fp32 partials that a separate
-//   log-sum-exp combine kernel merges.
+// * The plan gives each worker either whole tokens (few tokens of similar
+//   length) or a balanced contiguous range of the global tile list; split
+//   pieces write fp32 partials that a separate log-sum-exp combine kernel
+//   merges.
 //
-// Warp roles per CTA (224 threads): warp 0 = TMA producer, warp 1 = score
-// MMA issuer + TMEM owner, warp 6 = value MMA issuer (each issuer runs its
-// loop as a whole warp, one elected lane issues each batch of MMAs), warps
-// 2..5 = "row" warps, thread = head (TMEM lane).
+// Warp roles per CTA (384 threads): warp 0 = TMA producer, warp 1 = score
+// MMA issuer + TMEM owner, warp 2 = value MMA issuer (each issuer runs its
+// loop as a whole warp, one elected lane issues each batch of MMAs), warp 3 =
+// exchange issuer, warps 4..11 = softmax warps of 16 heads each (16-lane TMEM
+// shapes: thread t holds heads base + t/4 and base + t/4 + 8).  The softmax
+// warps report progress to the issuers through release/acquire counters in
+// shared memory; MMA completions reach them through mbarriers.
 // Every wait is bounded; a wait that runs out records MLA_ERR_DEVICE_TIMEOUT,
 // raises a CTA-wide abort flag and the roles drain and exit.
 #include <cuda.h>
@@ -640,14 +644,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kXchgWarp) {
     // ------------------------------------------------------------ exchange issuer
-    // Lane q ships row warp q's fp16 partial block of every tile to the same
-    // warp's inbox in the peer: once the block is written, and once the peer
+    // Lane rw ships softmax warp rw's fp16 partial block of every tile to the
+    // same warp's inbox in the peer: once the block is written, and once the peer
     // has consumed what it received into that inbox slot two tiles ago.  This
     // keeps the copy issue and its waits off the softmax warps' chain.
-    const int q = lane & (kRowWarps - 1);
-    const uint8_t* const outbox_q = smem + kOffOutbox + q * kXBlockBytes;
-    const uint32_t peer_inbox_q = map_to_rank(smem_u32(smem + kOffInbox + q * kXBlockBytes), peer);
-    const uint32_t peer_xin_q = map_to_rank(smem_u32(&bs->xin_full[0][q]), peer);
+    const int rw = lane & (kRowWarps - 1);
+    const uint8_t* const outbox_rw = smem + kOffOutbox + rw * kXBlockBytes;
+    const uint32_t peer_inbox_rw = map_to_rank(smem_u32(smem + kOffInbox + rw * kXBlockBytes), peer);
+    const uint32_t peer_xin_rw = map_to_rank(smem_u32(&bs->xin_full[0][rw]), peer);
     UnitIter iter = make_iter(p, g);
     Unit u;
     uint32_t i = 0;  // blocks shipped per row warp
@@ -658,12 +662,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t slot = i & 1;
         bool good = true;
         if (lane < kRowWarps) {
-          if (i >= 2) good = wait_bar(&bs->inbox_free[slot][q], ((i >> 1) - 1) & 1, p, bs, true);
+          if (i >= 2) good = wait_bar(&bs->inbox_free[slot][rw], ((i >> 1) - 1) & 1, p, bs, true);
           if (good) {
-            bulk_copy_to_peer(peer_inbox_q + slot * kXSlotBytes, outbox_q, kXBlockBytes, peer_xin_q + slot * kBarSlot);
+            bulk_copy_to_peer(peer_inbox_rw + slot * kXSlotBytes, outbox_rw, kXBlockBytes, peer_xin_rw + slot * kBarSlot);
             bulk_commit();
             bulk_wait_read<0>();
-            st_release_u32(&bs->n_out_free[q], i + 1);
+            st_release_u32(&bs->n_out_free[rw], i + 1);
           }
         }
         ok = __all_sync(0xffffffffu, good);
@@ -674,7 +678,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane < kRowWarps) {
       bulk_wait_all();
       for (uint32_t k = (i > 2 ? i - 2 : 0); ok && k < i; ++k)
-        ok = wait_bar(&bs->inbox_free[k & 1][q], (k >> 1) & 1, p, bs, true);
+        ok = wait_bar(&bs->inbox_free[k & 1][rw], (k >> 1) & 1, p, bs, true);
     }
   }
 
