@@ -255,7 +255,7 @@ def run_ours(args):
     m.check()
     ms = t0.elapsed_time(t1) / args.steps
     dec_ms = sum(a.elapsed_time(b) for a, b in dec_ev) / len(dec_ev)
-    launches_per_step = 3 + 1 + 1 + 3 + 2  # q_proj, append, absorb, plan+decode+combine, out
+    launches_per_step = 2 + 1 + 1 + 3 + 2  # q_proj (W^DQ; W^UQ and W^QR fused), append, absorb, plan+decode+combine, out
 
     # end to end through the public API with host buffers: H2D of the step's
     # inputs, the step, D2H of u -- all inside the timed region
