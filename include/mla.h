@@ -145,9 +145,12 @@ mla_status mla_absorb_q(mla_handle* h, const void* q_c, const void* q_r, const i
  *                     they sit at positions seq_lens[b]-q_len .. seq_lens[b]-1
  *                     and see rows 0..their own position (causal, inclusive)
  *   num_workers       0 = one worker per available SM pair; otherwise the
- *                     number of workers the keys are spread over.  Keys of a
- *                     token split across workers are merged by a log-sum-exp
- *                     combine (not on the pages).
+ *                     number of workers (two SMs each) launched.  On the
+ *                     device the plan gives each worker one whole token when
+ *                     there are no more tokens than workers and their key
+ *                     counts are close, else a balanced range of all keys;
+ *                     keys of a token split across workers are merged by a
+ *                     log-sum-exp combine (not on the pages).
  *   ws                mla_decode_workspace_bytes(h, n_tok, num_workers) bytes
  *   o_lat [n_tok, n_h, d_c]  (output, dims.dtype)   lse [n_tok, n_h] f32 (output)
  * n_tok must equal cu_q[batch] (checked on the device). */
