@@ -69,6 +69,38 @@ def _dist():
     return ws, rank
 
 
+def _init_dist(ws: int, backend: str = "nccl"):
+    """Joins the process group of a torchrun launch (nothing at N=1)."""
+    if ws > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend)
+
+
+def _barrier(ws: int, cuda: bool = True):
+    """All ranks meet, then this rank's device work drains."""
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if cuda:
+        torch.cuda.synchronize()
+
+
+def _max_over_ranks(vals, ws: int, device="cuda"):
+    """Element-wise maximum of the per-rank timings (every rank gets it)."""
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def _job_rate(units_per_rank: int, ws: int, ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed in one step over
+    the slowest rank's step time."""
+    return units_per_rank * ws / (ms * 1e-3)
+
+
 _SAMPLER = r"""
 import ctypes, sys, time
 lib = ctypes.CDLL("libnvidia-ml.so.1")
@@ -197,9 +229,7 @@ def run_ours(args):
     ws, rank = _dist()
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+    _init_dist(ws, "nccl")
     from head_latent_attention_26_b300 import build
     build.build()
     from head_latent_attention_26_b300 import mla
@@ -237,10 +267,7 @@ def run_ours(args):
     m.check()
 
     def barrier():
-        if ws > 1:
-            import torch.distributed as dist
-            dist.barrier()
-        torch.cuda.synchronize()
+        _barrier(ws)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -278,11 +305,7 @@ def run_ours(args):
     e2e_ms = e0.elapsed_time(e1) / args.steps
     m.check()
 
-    times = torch.tensor([ms, dec_ms, e2e_ms], dtype=torch.float64, device="cuda")
-    if ws > 1:
-        import torch.distributed as dist
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    ms, dec_ms, e2e_ms = times.tolist()
+    ms, dec_ms, e2e_ms = _max_over_ranks([ms, dec_ms, e2e_ms], ws)
     if rank != 0:
         return None
 
@@ -308,7 +331,7 @@ def run_ours(args):
                                                         "frac_burst": round(tflops / tf_burst, 4)}},
                 algorithmic_bytes=dec_bytes, algorithmic_flops=flops, decode_us=round(dec_ms * 1e3, 2))
     n = ws
-    value = B * n / (ms * 1e-3)
+    value = _job_rate(B, n, ms)
     res = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -328,9 +351,9 @@ def run_ours(args):
                    "parallelism": f"replicas x{n}" if n > 1 else "single GPU",
                    "l2": "no flush: the step reads > L2 (302 MB cache + 300 MB weights)"},
         "latent_cache_gbs": round(cache_b / t / 1e9, 1),
-        "decode_tokens_per_s": round(B * n / t, 1),
+        "decode_tokens_per_s": round(_job_rate(B, n, dec_ms), 1),
         "roofline": roof,
-        "e2e": {"value": round(B * n / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(_job_rate(B, n, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h_x.numel() * 2 + h_pos.numel() * 4 + h_lens.numel() * 4,
                 "d2h_bytes_per_step": h_u.numel() * 2},
         "gpu_launches": launches_per_step * args.steps,
