@@ -54,6 +54,8 @@ __all__ = [
     "attend_expanded",
     "output_projection",
     "absorb_query",
+    "absorbed_query_weight",
+    "latent_query_precomputed",
     "scores_latent",
     "attend_latent",
     "up_project",
@@ -240,6 +242,30 @@ def absorb_query(q_c, q_r, W_uk) -> np.ndarray:
     n_h, d_h = q_c.shape
     qt = np.stack([_head_rows(W_uk, i, d_h).T @ q_c[i] for i in range(n_h)])
     return np.concatenate([qt, q_r], axis=1)
+
+
+def absorbed_query_weight(W_uq, W_uk, n_h: int) -> np.ndarray:
+    """The query weight with W^UK folded in: W~^UQ_i = W^UK_i^T W^UQ_i.
+
+    [0h-n0] "行列吸収トリック": the product W^UK_i^T W^UQ_i can be formed once,
+    ahead of inference, after which the latent content query is a single
+    product of c^Q.  W_uq: [n_h*d_h, d_cq]; W_uk: [n_h*d_h, d_c].
+    Returns [n_h*d_c, d_cq]; rows [i*d_c, (i+1)*d_c) belong to head i.
+    """
+    W_uq, W_uk = f64(W_uq), f64(W_uk)
+    d_h = W_uq.shape[0] // n_h
+    return np.concatenate([_head_rows(W_uk, i, d_h).T @ _head_rows(W_uq, i, d_h) for i in range(n_h)])
+
+
+def latent_query_precomputed(c_q, W_uq_abs, q_r, n_h: int) -> np.ndarray:
+    """Latent query [W~^UQ_i c^Q ; q^R_i] for every head, straight from c^Q.
+
+    [0h-n0] "行列吸収トリック" with the folded weight of absorbed_query_weight.
+    c_q: [d_cq]; W_uq_abs: [n_h*d_c, d_cq]; q_r: [n_h, d_hr] (rotated).
+    Returns [n_h, d_c + d_hr].
+    """
+    qt = (f64(W_uq_abs) @ f64(c_q)).reshape(n_h, -1)
+    return np.concatenate([qt, f64(q_r)], axis=1)
 
 
 def scores_latent(q_lat_i, rows) -> np.ndarray:

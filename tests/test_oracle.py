@@ -51,6 +51,25 @@ def test_worked_example_both_orders():
     assert s_latent.tolist() == [g["score"]]
 
 
+def test_worked_example_precomputed_weight():
+    # The same example with the query itself produced by an up-projection:
+    # W^UQ = [[1,0],[0,1],[1,0]] maps c^Q = (1,2) to q = (1,2,1), so the folded
+    # weight W^UK^T W^UQ must send c^Q straight to U^T q = (2,3), and the
+    # score against c is 7 again.  The folded weight's entries are fixed by
+    # hand: folding in the other order, W^UQ^T W^UK, gives [[2,1],[0,1]].
+    g = _golden("worked_example.json")
+    U = np.array(g["U"], dtype=float)
+    W_uq = np.array([[1.0, 0.0], [0.0, 1.0], [1.0, 0.0]])
+    c_q = np.array([1.0, 2.0])
+    assert (W_uq @ c_q).tolist() == g["q"]
+    W_abs = O.absorbed_query_weight(W_uq, U, n_h=1)
+    assert W_abs.tolist() == [[2.0, 0.0], [1.0, 1.0]]
+    q_lat = O.latent_query_precomputed(c_q, W_abs, np.zeros((1, 0)), n_h=1)
+    assert q_lat[0].tolist() == g["Ut_q"]
+    assert O.scores_latent(q_lat[0], np.array([g["c"]], float)).tolist() == [g["score"]]
+    assert (W_uq.T @ U).tolist() == [[2.0, 1.0], [0.0, 1.0]]
+
+
 def test_worked_example_rejects_transposed_weight():
     # Using U^T where U belongs would change the answer (and the shapes).
     g = _golden("worked_example.json")
@@ -254,6 +273,38 @@ def test_absorbed_equals_expanded():
     o_abs = O.up_project(r["o_lat"], W["W_uv"])
     assert np.max(np.abs(o_abs - r["o"])) <= 1e-12 * np.max(np.abs(r["o"]))
     assert np.max(np.abs(r["lse_lat"] - r["lse"])) <= 1e-12 * max(1.0, np.max(np.abs(r["lse"])))
+
+
+def test_precomputed_query_equals_runtime_absorption():
+    # Two routes to the latent query: q^C = W^UQ c^Q then W^UK_i^T q^C_i per
+    # head, or the folded weight applied to c^Q.  Four heads with distinct
+    # weights, so a wrong head slice or a swapped operand shows.
+    W, rng = _random_layer(11)
+    h = rng.standard_normal((3, 32))
+    c_q, q_c, q_r_raw = O.query_parts(h, W["W_dq"], W["W_uq"], W["W_qr"], n_h=4)
+    W_abs = O.absorbed_query_weight(W["W_uq"], W["W_uk"], n_h=4)
+    assert W_abs.shape == (4 * 16, 24)
+    for n in range(3):
+        q_r = O.rope(q_r_raw[n], n + 5)
+        ref = O.absorb_query(q_c[n], q_r, W["W_uk"])
+        got = O.latent_query_precomputed(c_q[n], W_abs, q_r, n_h=4)
+        assert np.max(np.abs(got - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+def test_absorbed_query_weight_brute_force():
+    # every entry as an explicit scalar sum over the head's d_h rows
+    rng = np.random.default_rng(12)
+    n_h, d_h, d_c, d_cq = 3, 2, 4, 5
+    W_uq = rng.standard_normal((n_h * d_h, d_cq))
+    W_uk = rng.standard_normal((n_h * d_h, d_c))
+    got = O.absorbed_query_weight(W_uq, W_uk, n_h)
+    for i in range(n_h):
+        for c in range(d_c):
+            for k in range(d_cq):
+                s = 0.0
+                for e in range(d_h):
+                    s += W_uk[i * d_h + e][c] * W_uq[i * d_h + e][k]
+                assert abs(got[i * d_c + c][k] - s) <= 1e-13
 
 
 def test_merge_partials_equals_whole():
