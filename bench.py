@@ -305,7 +305,34 @@ def run_ours(args):
     e2e_ms = e0.elapsed_time(e1) / args.steps
     m.check()
 
-    ms, dec_ms, e2e_ms = _max_over_ranks([ms, dec_ms, e2e_ms], ws)
+    # the two routes to the latent query for the same tokens: runtime
+    # absorption (q_proj + absorb_q, the step above) and the folded weight
+    # W^UK_i^T W^UQ_i formed once ahead of time (q_proj_absorbed)
+    W_abs = m.absorb_weights(W["W_uq"], W["W_uk"])
+    q_lat_f = torch.empty_like(bufs["q_lat"])
+    n_q = max(3, min(args.steps, 300))
+
+    def time_route(fn):
+        for _ in range(3):
+            fn()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n_q):
+            fn()
+        b.record()
+        barrier()
+        return a.elapsed_time(b) / n_q
+
+    def runtime_route():
+        m.q_proj(inp["x"], W["W_dq"], W["W_uq"], W["W_qr"], bufs["q_c"], bufs["q_r"])
+        m.absorb_q(bufs["q_c"], bufs["q_r"], inp["pos"], W["W_uk"], bufs["q_lat"])
+
+    rt_ms = time_route(runtime_route)
+    fold_ms = time_route(lambda: m.q_proj_absorbed(inp["x"], W["W_dq"], W_abs, W["W_qr"], inp["pos"], q_lat_f))
+    m.check()
+    del W_abs
+    ms, dec_ms, e2e_ms, rt_ms, fold_ms = _max_over_ranks([ms, dec_ms, e2e_ms, rt_ms, fold_ms], ws)
     if rank != 0:
         return None
 
@@ -356,6 +383,12 @@ def run_ours(args):
         "e2e": {"value": round(_job_rate(B, n, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h_x.numel() * 2 + h_pos.numel() * 4 + h_lens.numel() * 4,
                 "d2h_bytes_per_step": h_u.numel() * 2},
+        "query_routes": {"runtime_absorb_us": round(rt_ms * 1e3, 2), "folded_weight_us": round(fold_ms * 1e3, 2),
+                         "weight_bytes": {"runtime": 2 * d.d_cq * (d.d_model + d.n_h * (d.d_h + d.d_hr))
+                                          + 2 * d.n_h * d.d_h * d.d_c,
+                                          "folded": 2 * d.d_cq * (d.d_model + d.n_h * (d.d_c + d.d_hr))},
+                         "note": "W^DQ, W^UQ + W^QR, W^UK absorb (runtime) vs W^DQ, folded W^UK_i^T W^UQ_i + W^QR "
+                                 f"(one launch), {n_q} back-to-back calls each, outside the timed step"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }

@@ -102,6 +102,11 @@ cudaError_t launch_cache_append_simt(const mla_handle* h, const void* x, const v
                                      int n_pool_blocks, cudaStream_t s);
 cudaError_t launch_absorb_q_simt(const mla_handle* h, const void* q_c, const void* q_r, const int* pos,
                                  int n_tok, const void* w_uk, void* q_lat, cudaStream_t s);
+// W~^UQ_i = W^UK_i^T W^UQ_i for every head (any dims, fp32 sums)
+cudaError_t launch_absorb_weights(const mla_handle* h, const void* w_uq, const void* w_uk, void* w_abs,
+                                  cudaStream_t s);
+cudaError_t launch_q_absorbed_simt(const mla_handle* h, const void* c_q, const void* w_abs, const void* w_qr,
+                                   const int* pos, int n_tok, void* q_lat, cudaStream_t s);
 cudaError_t launch_decode_simt(const mla_handle* h, const void* q_lat, const void* pool,
                                int n_pool_blocks, const int* block_table, int max_blocks,
                                const int* seq_lens, const int* cu_q, int batch, int n_tok, void* o_lat,
@@ -129,6 +134,10 @@ cudaError_t launch_linear2_tc(const mla_handle* h, const void* X, int in, const 
 cudaError_t launch_cache_append_tc(const mla_handle* h, const void* x, const void* w_dkr, const int* seq_idx,
                                    const int* pos, int n_new, const int* block_table, int max_blocks, int batch,
                                    void* pool, int n_pool_blocks, cudaStream_t s);
+// Latent query from c^Q with the folded weight: [W~^UQ c^Q ; RoPE_pos(W^QR c^Q)]
+// straight into q_lat, both products in one launch.
+cudaError_t launch_q_absorbed_tc(const mla_handle* h, const void* c_q, const void* w_abs, const void* w_qr,
+                                 const int* pos, int n_tok, void* q_lat, cudaStream_t s);
 cudaError_t launch_absorb_q_tc(const mla_handle* h, const void* q_c, const void* q_r, const int* pos, int n_tok,
                                const void* w_uk, void* q_lat, cudaStream_t s);
 // Same kernels with their scratch in a fixed device array (no allocation).

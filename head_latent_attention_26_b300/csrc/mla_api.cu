@@ -183,6 +183,36 @@ mla_status mla_absorb_q(mla_handle* h, const void* q_c, const void* q_r, const i
   return MLA_OK;
 }
 
+// ---------------------------------------------------------------- folded query weight
+mla_status mla_absorb_weights(mla_handle* h, const void* w_uq, const void* w_uk, void* w_uq_abs,
+                              cudaStream_t stream) {
+  if (!h) return MLA_ERR_INVALID_ARG;
+  for (const void* p : {w_uq, w_uk, static_cast<const void*>(w_uq_abs)})
+    if (!p || !aligned16(p)) return MLA_ERR_INVALID_ARG;
+  MLA_TRY_CUDA(mla::launch_absorb_weights(h, w_uq, w_uk, w_uq_abs, stream));
+  return MLA_OK;
+}
+
+mla_status mla_q_proj_absorbed(mla_handle* h, const void* x, const void* w_dq, const void* w_uq_abs,
+                               const void* w_qr, const int* pos, int n_tok, void* q_lat, void* ws,
+                               size_t ws_bytes, cudaStream_t stream) {
+  if (!h || n_tok < 0) return MLA_ERR_INVALID_ARG;
+  if (n_tok == 0) return MLA_OK;
+  for (const void* p : {x, w_dq, w_uq_abs, w_qr, static_cast<const void*>(q_lat)})
+    if (!p || !aligned16(p)) return MLA_ERR_INVALID_ARG;
+  if (!pos || !aligned4(pos)) return MLA_ERR_INVALID_ARG;
+  if (!ws || !aligned16(ws) || ws_bytes < mla_q_proj_workspace_bytes(h, n_tok)) return MLA_ERR_WORKSPACE;
+  const mla_dims& d = h->dims;
+  if (h->proj_tc) {
+    MLA_TRY_CUDA(mla::launch_linear_tc(h, x, d.d_model, w_dq, d.d_model, d.d_cq, 1, 0, ws, d.d_cq, n_tok, stream));
+    MLA_TRY_CUDA(mla::launch_q_absorbed_tc(h, ws, w_uq_abs, w_qr, pos, n_tok, q_lat, stream));
+    return MLA_OK;
+  }
+  MLA_TRY_CUDA(mla::launch_linear(h, x, d.d_model, w_dq, d.d_model, d.d_cq, ws, d.d_cq, n_tok, stream));
+  MLA_TRY_CUDA(mla::launch_q_absorbed_simt(h, ws, w_uq_abs, w_qr, pos, n_tok, q_lat, stream));
+  return MLA_OK;
+}
+
 // ---------------------------------------------------------------- a3 + a4
 size_t mla_decode_workspace_bytes(const mla_handle* h, int n_tok, int num_workers) {
   if (!h || n_tok < 0 || num_workers < 0) return 0;

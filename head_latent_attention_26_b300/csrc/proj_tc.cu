@@ -24,7 +24,11 @@
 //   bf16 and written to pool row block_table[b][pos/64]*64 + pos%64;
 // * absorb: q~_i = W^UK_i^T q^C_i ([0h-n0] "行列吸収トリック") with the W^UK
 //   tile read as an MN-major A operand (no transpose copy), plus the RoPE of
-//   q^R_i, written as one latent query row [q~_i ; RoPE_pos(q^R_i)].
+//   q^R_i, written as one latent query row [q~_i ; RoPE_pos(q^R_i)];
+// * folded query: the same latent query row straight from c^Q with the
+//   folded weight W~^UQ_i = W^UK_i^T W^UQ_i ([0h-n0] "行列吸収トリック": the
+//   product can be formed ahead of inference) as the first product and W^QR
+//   as the second, rotated in the epilogue.
 //
 // [0h-n0] = "論文解説: DeepSeek-V2 — … Multi-head Latent Attention",
 // [qiita] = MLA notes on qiita.com, [kasblo] = MLA explainer on kasblo.com.
@@ -48,7 +52,7 @@ constexpr int kThreads = 128;
 constexpr int kMaxSplit = 16;                  // cluster size (above 8 needs the non-portable opt-in)
 constexpr int kMaxDevices = 16;                // devices whose resident-cluster counts are cached
 
-enum : int { kModeLinear = 0, kModeAppend = 1, kModeAbsorb = 2 };
+enum : int { kModeLinear = 0, kModeAppend = 1, kModeAbsorb = 2, kModeQFolded = 3 };
 
 struct ProjMaps {
   CUtensorMap w;   // weights
@@ -127,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
   const int n0 = blockIdx.z * NT;
   // first output tile of this CTA; in linear mode tiles past seg1_tiles are
   // tiles of the second product
-  const bool seg2 = MODE == kModeLinear && static_cast<int>(blockIdx.y) * MT >= p.seg1_tiles;
+  const bool seg2 = (MODE == kModeLinear || MODE == kModeQFolded) && static_cast<int>(blockIdx.y) * MT >= p.seg1_tiles;
   const int tile0 = static_cast<int>(blockIdx.y) * MT - (seg2 ? p.seg1_tiles : 0);
   const CUtensorMap* wmap = seg2 ? &maps.w2 : &maps.w;
   const int group = tile0 / p.tiles_per_group;  // all MT tiles share it (MT divides tiles_per_group)
@@ -330,6 +334,25 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
               const size_t t = static_cast<size_t>(ss->tpos[c0 + col]) * half + k;
               const float cs = __ldg(p.rope_cos + t), sn = __ldg(p.rope_sin + t);
               store_pair(dst, a.x * cs - a.y * sn, a.x * sn + a.y * cs);
+            }
+          } else if (MODE == kModeQFolded) {
+            const int o = o_tile * kBM + row;
+            if (!seg2) {
+              // W~^UQ row o = latent column o % d_c of head o / d_c
+              if (o < p.out)
+                store_pair(p.q_lat + (static_cast<size_t>(n) * p.n_h + o / p.d_c) * p.width + o % p.d_c, a.x, a.y);
+            } else if (o < p.out2) {
+              // W^QR row o = positional column o % d_hr of head o / d_hr: rotate the pair
+              const int tp = __ldg(p.pos + n);
+              if (tp < 0 || tp >= p.max_pos) {
+                report(p.status, MLA_ERR_DEVICE_BOUNDS);
+                continue;
+              }
+              const int k2 = o % p.d_hr;
+              const size_t t = static_cast<size_t>(tp) * half + (k2 >> 1);
+              const float cs = __ldg(p.rope_cos + t), sn = __ldg(p.rope_sin + t);
+              store_pair(p.q_lat + (static_cast<size_t>(n) * p.n_h + o / p.d_hr) * p.width + p.d_c + k2,
+                         a.x * cs - a.y * sn, a.x * sn + a.y * cs);
             }
           } else {
             const int o = (o_tile % p.tiles_per_group) * kBM + row;  // latent column of head `group`
@@ -558,6 +581,25 @@ cudaError_t launch_linear2_tc(const mla_handle* h, const void* X, int in, const 
   p.ldy2 = ldy2;
   p.seg1_tiles = t1;
   return launch_proj<kModeLinear, 1>(maps, p, pick_split(h, t1 + t2, n_tok, p.k_blocks), t1 + t2, h->num_sms, s);
+}
+
+cudaError_t launch_q_absorbed_tc(const mla_handle* h, const void* c_q, const void* w_abs, const void* w_qr,
+                                 const int* pos, int n_tok, void* q_lat, cudaStream_t s) {
+  const mla_dims& d = h->dims;
+  const int out1 = d.n_h * d.d_c, out2 = d.n_h * d.d_hr;
+  ProjMaps maps;
+  if (!encode_bf16_2d(&maps.w, w_abs, d.d_cq, out1, kBK, kBM) || !encode_bf16_2d(&maps.w2, w_qr, d.d_cq, out2, kBK, kBM) ||
+      !encode_bf16_2d(&maps.x, c_q, d.d_cq, n_tok, kBK, token_tile(n_tok)))
+    return cudaErrorInvalidValue;
+  ProjParams p = base_params(h, n_tok);
+  const int t1 = (out1 + kBM - 1) / kBM, t2 = (out2 + kBM - 1) / kBM;
+  p.out = out1;
+  p.out2 = out2;
+  p.k_blocks = (d.d_cq + kBK - 1) / kBK;
+  p.seg1_tiles = t1;
+  p.pos = pos;
+  p.q_lat = static_cast<__nv_bfloat16*>(q_lat);
+  return launch_proj<kModeQFolded, 1>(maps, p, pick_split(h, t1 + t2, n_tok, p.k_blocks), t1 + t2, h->num_sms, s);
 }
 
 cudaError_t launch_cache_append_tc(const mla_handle* h, const void* x, const void* w_dkr, const int* seq_idx,

@@ -122,6 +122,102 @@ __global__ void __launch_bounds__(256) absorb_q_kernel(const T* __restrict__ q_c
   }
 }
 
+// Folded query weight W~^UQ_i = W^UK_i^T W^UQ_i ([0h-n0] "行列吸収トリック":
+// formed once, ahead of inference): Wt[i*d_c + c, k] = sum_e W_uk[i*d_h + e, c]
+// W_uq[i*d_h + e, k], fp32 sums rounded once.  One 64 x 64 output tile of one
+// head per block (blockIdx.z = head); 16 x 16 threads, 4 x 4 outputs each,
+// both operand tiles staged through shared memory 16 rows of e at a time.
+template <typename T>
+__global__ void __launch_bounds__(256) absorb_weights_kernel(const T* __restrict__ w_uq,
+                                                             const T* __restrict__ w_uk, T* __restrict__ w_abs,
+                                                             int d_h, int d_c, int d_cq) {
+  __shared__ float a[16][64];  // W_uk rows e, latent columns c
+  __shared__ float b[16][64];  // W_uq rows e, input columns k
+  const int i = blockIdx.z;
+  const int c0 = blockIdx.y * 64, k0 = blockIdx.x * 64;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4] = {};
+  const T* uk = w_uk + static_cast<size_t>(i) * d_h * d_c;
+  const T* uq = w_uq + static_cast<size_t>(i) * d_h * d_cq;
+  for (int e0 = 0; e0 < d_h; e0 += 16) {
+    for (int f = threadIdx.x; f < 16 * 64; f += 256) {
+      const int e = e0 + f / 64, col = f % 64;
+      a[f / 64][col] = (e < d_h && c0 + col < d_c) ? to_f(uk[static_cast<size_t>(e) * d_c + c0 + col]) : 0.f;
+      b[f / 64][col] = (e < d_h && k0 + col < d_cq) ? to_f(uq[static_cast<size_t>(e) * d_cq + k0 + col]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        av[r] = a[e][ty * 4 + r];
+        bv[r] = b[e][tx * 4 + r];
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[r][q] = fmaf(av[r], bv[q], acc[r][q]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int c = c0 + ty * 4 + r;
+    if (c >= d_c) continue;
+    T* dst = w_abs + (static_cast<size_t>(i) * d_c + c) * d_cq;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (k0 + tx * 4 + q < d_cq) dst[k0 + tx * 4 + q] = from_f<T>(acc[r][q]);
+  }
+}
+
+// One block per (head, token): the latent query straight from c^Q with the
+// folded weight, [W~^UQ_i c^Q ; RoPE_pos(W^QR_i c^Q)] ([0h-n0] "行列吸収トリック",
+// [qiita] "RoPE の扱い"), one warp per output feature.
+template <typename T>
+__global__ void __launch_bounds__(256) q_absorbed_kernel(const T* __restrict__ c_q, const T* __restrict__ w_abs,
+                                                         const T* __restrict__ w_qr, const int* __restrict__ pos,
+                                                         T* __restrict__ q_lat, int n_h, int d_cq, int d_hr,
+                                                         int d_c, const float* __restrict__ rope_cos,
+                                                         const float* __restrict__ rope_sin, int max_pos,
+                                                         int* status) {
+  extern __shared__ float sh[];  // c^Q [d_cq], then the raw positional query [d_hr]
+  float* cq = sh;
+  float* qr = sh + d_cq;
+  const int i = blockIdx.x, n = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int k = threadIdx.x; k < d_cq; k += blockDim.x) cq[k] = to_f(c_q[static_cast<size_t>(n) * d_cq + k]);
+  __syncthreads();
+  const size_t hn = static_cast<size_t>(n) * n_h + i;
+  T* out = q_lat + hn * (d_c + d_hr);
+  for (int o = warp; o < d_c + d_hr; o += 8) {
+    const T* w = o < d_c ? w_abs + (static_cast<size_t>(i) * d_c + o) * d_cq
+                         : w_qr + (static_cast<size_t>(i) * d_hr + (o - d_c)) * d_cq;
+    float acc = 0.f;
+    for (int k = lane; k < d_cq; k += 32) acc = fmaf(to_f(w[k]), cq[k], acc);
+    acc = warp_sum(acc);
+    if (lane == 0) {
+      if (o < d_c) out[o] = from_f<T>(acc);
+      else qr[o - d_c] = acc;
+    }
+  }
+  __syncthreads();
+  const int p = pos[n];
+  if (p < 0 || p >= max_pos) {
+    if (threadIdx.x == 0) report(status, MLA_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  const int half = d_hr / 2;
+  for (int k = threadIdx.x; k < half; k += blockDim.x) {
+    const float c = rope_cos[static_cast<size_t>(p) * half + k];
+    const float s = rope_sin[static_cast<size_t>(p) * half + k];
+    const float x0 = qr[2 * k], x1 = qr[2 * k + 1];
+    out[d_c + 2 * k] = from_f<T>(x0 * c - x1 * s);
+    out[d_c + 2 * k + 1] = from_f<T>(x0 * s + x1 * c);
+  }
+}
+
 // One block (4 warps) per (token, head).  Warp w takes keys j = w, w+4, ...
 // up to the token's position, keeps a running max / sum / weighted latent sum
 // (online softmax), and the four warps are merged at the end.
@@ -265,6 +361,32 @@ cudaError_t launch_absorb_q_simt(const mla_handle* h, const void* q_c, const voi
                       static_cast<const T*>(q_c), static_cast<const T*>(q_r), pos,
                       static_cast<const T*>(w_uk), static_cast<T*>(q_lat), d.n_h, d.d_h, d.d_hr,
                       d.d_c, h->rope_cos, h->rope_sin, h->max_pos, h->status)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_absorb_weights(const mla_handle* h, const void* w_uq, const void* w_uk, void* w_abs,
+                                  cudaStream_t s) {
+  const mla_dims& d = h->dims;
+  dim3 grid((d.d_cq + 63) / 64, (d.d_c + 63) / 64, d.n_h);
+  MLA_DISPATCH(h, (absorb_weights_kernel<T><<<grid, 256, 0, s>>>(
+                      static_cast<const T*>(w_uq), static_cast<const T*>(w_uk), static_cast<T*>(w_abs), d.d_h,
+                      d.d_c, d.d_cq)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_q_absorbed_simt(const mla_handle* h, const void* c_q, const void* w_abs, const void* w_qr,
+                                   const int* pos, int n_tok, void* q_lat, cudaStream_t s) {
+  const mla_dims& d = h->dims;
+  dim3 grid(d.n_h, n_tok);
+  const size_t smem = sizeof(float) * (d.d_cq + d.d_hr);
+  if (smem > 48 * 1024) {
+    MLA_DISPATCH(h, (cudaFuncSetAttribute(q_absorbed_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(smem))));
+  }
+  MLA_DISPATCH(h, (q_absorbed_kernel<T><<<grid, 256, smem, s>>>(
+                      static_cast<const T*>(c_q), static_cast<const T*>(w_abs), static_cast<const T*>(w_qr), pos,
+                      static_cast<T*>(q_lat), d.n_h, d.d_cq, d.d_hr, d.d_c, h->rope_cos, h->rope_sin,
+                      h->max_pos, h->status)));
   return cudaGetLastError();
 }
 

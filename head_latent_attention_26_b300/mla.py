@@ -58,6 +58,8 @@ _SIGS = {
     "mla_q_proj": (I, [P, P, P, P, P, I, P, P, P, SZ, P]),
     "mla_cache_append": (I, [P, P, P, P, P, I, P, I, I, P, I, P]),
     "mla_absorb_q": (I, [P, P, P, P, I, P, P, P]),
+    "mla_absorb_weights": (I, [P, P, P, P, P]),
+    "mla_q_proj_absorbed": (I, [P, P, P, P, P, P, I, P, P, SZ, P]),
     "mla_decode_workspace_bytes": (SZ, [P, I, I]),
     "mla_decode": (I, [P, P, P, I, P, I, P, P, I, I, I, P, SZ, P, P, P]),
     "mla_decode_noalloc": (I, [P, P, P, I, P, I, P, P, I, I, I, P, P, P]),
@@ -184,6 +186,26 @@ class MLA:
         q_lat = torch.empty(n, d.n_h, d.width, dtype=self.dtype, device=q_c.device) if q_lat is None else q_lat
         _check(self.lib.mla_absorb_q(self.h, _ptr(q_c), _ptr(q_r), _ptr(pos), n, _ptr(W_uk), _ptr(q_lat),
                                      P(_stream())), "mla_absorb_q")
+        return q_lat
+
+    def absorb_weights(self, W_uq, W_uk, W_uq_abs=None):
+        """The folded query weight W^UK_i^T W^UQ_i of every head, [n_h*d_c, d_cq]."""
+        d = self.dims
+        if W_uq_abs is None:
+            W_uq_abs = torch.empty(d.n_h * d.d_c, d.d_cq, dtype=self.dtype, device=W_uq.device)
+        _check(self.lib.mla_absorb_weights(self.h, _ptr(W_uq), _ptr(W_uk), _ptr(W_uq_abs), P(_stream())),
+               "mla_absorb_weights")
+        return W_uq_abs
+
+    def q_proj_absorbed(self, x, W_dq, W_uq_abs, W_qr, pos, q_lat=None):
+        """The latent query straight from x with the folded weight (replaces
+        q_proj + absorb_q)."""
+        d, n = self.dims, x.shape[0]
+        q_lat = torch.empty(n, d.n_h, d.width, dtype=self.dtype, device=x.device) if q_lat is None else q_lat
+        nb = self.lib.mla_q_proj_workspace_bytes(self.h, n)
+        ws = self.workspace("q_proj", nb)
+        _check(self.lib.mla_q_proj_absorbed(self.h, _ptr(x), _ptr(W_dq), _ptr(W_uq_abs), _ptr(W_qr), _ptr(pos), n,
+                                            _ptr(q_lat), _ptr(ws), ws.numel(), P(_stream())), "mla_q_proj_absorbed")
         return q_lat
 
     def decode_workspace_bytes(self, n_tok: int, num_workers: int = 0) -> int:

@@ -133,6 +133,31 @@ mla_status mla_cache_append(mla_handle* h, const void* x, const void* w_dkr, con
 mla_status mla_absorb_q(mla_handle* h, const void* q_c, const void* q_r, const int* pos,
                         int n_tok, const void* w_uk, void* q_lat, cudaStream_t stream);
 
+/* ---- a0 + a2 with the folded query weight ----------------------------------
+ * [0h-n0] "行列吸収トリック": W~^UQ_i = W^UK_i^T W^UQ_i can be formed once,
+ * ahead of inference; the latent content query is then the single product
+ * W~^UQ_i c^Q, and no q^C is formed.
+ *
+ * mla_absorb_weights forms the folded weight (a preparation step, not part
+ * of the decode step): fp32 sums over the head's d_h rows, rounded once.
+ *   w_uq [n_h*d_h, d_cq]   w_uk [n_h*d_h, d_c]
+ *   w_uq_abs [n_h*d_c, d_cq]  (output; rows [i*d_c, (i+1)*d_c) = head i)
+ *
+ * mla_q_proj_absorbed replaces mla_q_proj + mla_absorb_q:
+ * c^Q = W^DQ x, then q_lat = [W~^UQ_i c^Q ; RoPE_pos(W^QR_i c^Q)].
+ *   x [n_tok, d_model]   w_dq [d_cq, d_model]   w_uq_abs as above
+ *   w_qr [n_h*d_hr, d_cq]   pos [n_tok] int32 (0-based positions)
+ *   q_lat [n_tok, n_h, d_c + d_hr]  (output, the layout mla_decode reads)
+ *   ws: mla_q_proj_workspace_bytes(h, n_tok) bytes (holds c^Q).
+ * A position outside [0, max_pos) leaves that token's positional part
+ * unwritten and sets MLA_ERR_DEVICE_BOUNDS.  Which is faster depends on
+ * n_tok: the folded weight is d_c/d_h = 4 times the size of W^UQ. */
+mla_status mla_absorb_weights(mla_handle* h, const void* w_uq, const void* w_uk, void* w_uq_abs,
+                              cudaStream_t stream);
+mla_status mla_q_proj_absorbed(mla_handle* h, const void* x, const void* w_dq, const void* w_uq_abs,
+                               const void* w_qr, const int* pos, int n_tok, void* q_lat, void* ws,
+                               size_t ws_bytes, cudaStream_t stream);
+
 /* ---- a3 + a4: latent attention over the paged cache -----------------------
  * [qiita] "Attention 計算" in absorbed form: s_ij = scale*(q~_i.c_j + q^R_i.k^R_j)
  * for every cached row j <= t (t = the query's position), softmax over j,

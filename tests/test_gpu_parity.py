@@ -419,3 +419,66 @@ def test_v2_absorb_q_token_tiles(v2, n_tok):
     for n in sorted({0, n_tok // 2, n_tok - 1}):
         ref = O.absorb_query(to_np(q_c[n]), O.rope(to_np(q_r[n]), int(pos[n]), d.rope_base), to_np(W["W_uk"]))
         assert row_rel_err(to_np(q_lat[n]), ref) < OUT_TOL, n
+
+
+# ---------------------------------------------------------------------------
+# Folded query weight W~^UQ_i = W^UK_i^T W^UQ_i and the latent query from c^Q
+# ---------------------------------------------------------------------------
+
+def test_tiny_folded_query(tiny):
+    d, n = TINY, 5
+    W = synth.weights(d, 1050, dtype=torch.float32, device="cuda")
+    x = synth.hidden(n, d, 1050, dtype=torch.float32, device="cuda")
+    pos = torch.tensor([0, 1, 17, 40, 63], dtype=torch.int32, device="cuda")
+    W_abs = tiny.absorb_weights(W["W_uq"], W["W_uk"])
+    q_lat = tiny.q_proj_absorbed(x, W["W_dq"], W_abs, W["W_qr"], pos)
+    tiny.check()
+    Wn = _np_weights(W)
+    W_abs_ref = O.absorbed_query_weight(Wn["W_uq"], Wn["W_uk"], d.n_h)
+    assert row_rel_err(to_np(W_abs), W_abs_ref) < 1e-5
+    c_q, q_c, q_r_raw = O.query_parts(to_np(x), Wn["W_dq"], Wn["W_uq"], Wn["W_qr"], d.n_h)
+    for i in range(n):
+        q_r = O.rope(q_r_raw[i], int(pos[i]), d.rope_base)
+        ref = O.latent_query_precomputed(c_q[i], W_abs_ref, q_r, d.n_h)
+        # the same latent query by the runtime route
+        assert np.max(np.abs(ref - O.absorb_query(q_c[i], q_r, Wn["W_uk"]))) <= 1e-12 * np.max(np.abs(ref))
+        assert row_rel_err(to_np(q_lat[i]), ref) < 1e-4, i
+
+
+def test_v2_folded_weight(v2):
+    d = V2
+    W = synth.weights(d, 1051, device="cuda")
+    W_abs = v2.absorb_weights(W["W_uq"], W["W_uk"])
+    v2.check()
+    assert W_abs.shape == (d.n_h * d.d_c, d.d_cq)
+    W_uq, W_uk = to_np(W["W_uq"]), to_np(W["W_uk"])
+    for i in (0, 1, 77, 127):
+        rows = slice(i * d.d_h, (i + 1) * d.d_h)
+        ref = O.absorbed_query_weight(W_uq[rows], W_uk[rows], 1)
+        got = to_np(W_abs[i * d.d_c:(i + 1) * d.d_c])
+        # fp32 sums of 128 products rounded once to bf16
+        assert row_rel_err(got, ref) < 1e-2, i
+        assert np.max(np.abs(got - ref)) <= 2 ** -8 * np.max(np.abs(ref)), i
+
+
+@pytest.mark.parametrize("n_tok", [1, 64, 100, 300])
+def test_v2_q_proj_absorbed_token_tiles(v2, n_tok):
+    d = V2
+    seed = 1060 + n_tok
+    W = synth.weights(d, seed, device="cuda")
+    x = synth.hidden(n_tok, d, seed, device="cuda")
+    pos = torch.randint(0, MAX_POS, (n_tok,), generator=torch.Generator().manual_seed(seed),
+                        dtype=torch.int32).cuda()
+    W_abs = v2.absorb_weights(W["W_uq"], W["W_uk"])
+    q_lat = v2.q_proj_absorbed(x, W["W_dq"], W_abs, W["W_qr"], pos)
+    # the runtime route on the same inputs, for the same tokens
+    q_c, q_r = v2.q_proj(x, W["W_dq"], W["W_uq"], W["W_qr"])
+    q_lat_rt = v2.absorb_q(q_c, q_r, pos, W["W_uk"])
+    v2.check()
+    Wn = _np_weights(W)
+    picks = sorted({0, n_tok // 3, n_tok // 2, n_tok - 1})
+    c_q, q_c_ref, q_r_raw = O.query_parts(to_np(x[picks]), Wn["W_dq"], Wn["W_uq"], Wn["W_qr"], d.n_h)
+    for j, n in enumerate(picks):
+        ref = O.absorb_query(q_c_ref[j], O.rope(q_r_raw[j], int(pos[n]), d.rope_base), Wn["W_uk"])
+        assert row_rel_err(to_np(q_lat[n]), ref) < OUT_TOL, n
+        assert row_rel_err(to_np(q_lat_rt[n]), ref) < OUT_TOL, n
