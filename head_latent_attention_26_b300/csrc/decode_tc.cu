@@ -143,6 +143,8 @@ constexpr uint32_t kBarSlot = kRowWarps * sizeof(uint64_t);  // stride of one sl
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Params& p, Bars* bs,
                                          bool cluster_scope = false) {
+  // an already completed phase is seen by the cheaper non-blocking test
+  if (cluster_scope ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity)) return true;
   for (long long i = 0;; ++i) {
     if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (i >= p.wait_limit || *reinterpret_cast<volatile int*>(&bs->abort)) {
