@@ -56,6 +56,11 @@ __all__ = [
     "absorb_query",
     "absorbed_query_weight",
     "latent_query_precomputed",
+    "Q8_BLOCK",
+    "quantize_q8_blocks",
+    "dequantize_q8_blocks",
+    "quantize_cache_rows",
+    "dequantize_cache_rows",
     "scores_latent",
     "attend_latent",
     "up_project",
@@ -298,6 +303,67 @@ def attend_latent(q_lat, rows, d_c: int, d_h: int, heads=None):
         o.append(a @ rows[:, :d_c])
         lse.append(l)
     return np.array(o), np.array(lse)
+
+
+# --------------------------------------------------------------------------
+# Quantised latent cache (int8 codes in blocks with one fp16 scale)
+# --------------------------------------------------------------------------
+
+Q8_BLOCK = 32
+
+
+def quantize_q8_blocks(x, block: int = Q8_BLOCK):
+    """int8 block codes of cached latent values.
+
+    [0h-n0] "量子化との組み合わせ": the compressed c^KV can be stored further
+    with KV-cache quantisation of the Q8_0 kind (llama.cpp's q8_0 cache type).
+    The page names the format only; the reading taken is that format's
+    definition: each run of `block` consecutive values shares one scale
+    d = max|x| / 127 kept in fp16, and each value becomes the int8 code
+    round(x / d), nearest with ties away from zero; an all-zero block has
+    d = 0 and codes 0.  The scale and the codes are decided in fp32 (x and the
+    fp16 scale widened to fp32, one correctly rounded fp32 division), the
+    precision a GPU kernel would use, so both sides reach the same integers.
+
+    x: [..., n] with n a multiple of `block`, values exact in fp32 and below
+    127 * 65504 in magnitude.  Returns codes int8 [..., n] and scales float16
+    [..., n / block].
+    """
+    x32 = np.asarray(x, dtype=np.float32)
+    shp = x32.shape
+    blocks = x32.reshape(shp[:-1] + (shp[-1] // block, block))
+    amax = np.max(np.abs(blocks), axis=-1)
+    d16 = (amax / np.float32(127.0)).astype(np.float16)
+    d32 = d16.astype(np.float32)[..., None]
+    safe = np.where(d32 > 0, d32, np.float32(1.0))
+    v = np.where(d32 > 0, blocks / safe, np.float32(0.0)).astype(np.float32)
+    q = np.sign(v) * np.floor(np.abs(v) + np.float32(0.5))
+    return np.clip(q, -127, 127).astype(np.int8).reshape(shp), d16
+
+
+def dequantize_q8_blocks(q, d, block: int = Q8_BLOCK) -> np.ndarray:
+    """The values a quantised block stands for: code x scale (exact in float64)."""
+    q64 = np.asarray(q, dtype=np.float64)
+    shp = q64.shape
+    d64 = np.asarray(d, dtype=np.float64)[..., None]
+    return (q64.reshape(shp[:-1] + (shp[-1] // block, block)) * d64).reshape(shp)
+
+
+def quantize_cache_rows(rows, d_c: int, block: int = Q8_BLOCK):
+    """A cache of rows [c^KV ; k^R] with c^KV quantised and k^R kept as is.
+
+    The positional key is shared by all heads and carries the rotation, so
+    only the d_c latent values are quantised.  rows: [T, d_c + d_hr].
+    Returns (codes int8 [T, d_c], scales float16 [T, d_c / block], k_r [T, d_hr]).
+    """
+    rows = np.asarray(rows)
+    q, d = quantize_q8_blocks(rows[:, :d_c], block)
+    return q, d, rows[:, d_c:]
+
+
+def dequantize_cache_rows(q, d, k_r, block: int = Q8_BLOCK) -> np.ndarray:
+    """Rows [dequantised c^KV ; k^R] in float64, the input attend_latent takes."""
+    return np.concatenate([dequantize_q8_blocks(q, d, block), f64(k_r)], axis=1)
 
 
 def up_project(o_lat, W_uv) -> np.ndarray:

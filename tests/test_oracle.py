@@ -307,6 +307,70 @@ def test_absorbed_query_weight_brute_force():
                 assert abs(got[i * d_c + c][k] - s) <= 1e-13
 
 
+# --------------------------------------------------------------------------
+# Quantised latent cache: block codes
+# --------------------------------------------------------------------------
+
+def test_q8_exact_block():
+    # codes k with scale 2^-4: the largest |x| is 127 * 2^-4, so d = 2^-4
+    # exactly and every value comes back unchanged
+    k = np.array([-127, -100, -64, -33, -17, -8, -5, -3, -2, -1, 0, 0, 1, 2, 3, 4,
+                  5, 6, 7, 9, 12, 15, 20, 31, 32, 47, 63, 64, 90, 111, 126, 127])
+    x = k * 2.0 ** -4
+    q, d = O.quantize_q8_blocks(x[None])
+    assert q.dtype == np.int8 and d.dtype == np.float16
+    assert q[0].tolist() == k.tolist() and d.tolist() == [[2.0 ** -4]]
+    assert O.dequantize_q8_blocks(q, d)[0].tolist() == x.tolist()
+
+
+def test_q8_zero_block_and_ties():
+    x = np.zeros((1, 64))
+    # second block: largest 127/16, then exact half-way values 2.5, 0.5 and -1.5
+    # (in units of the scale 1/16): ties go away from zero (3, 1, -2), which
+    # round-half-to-even would send to 2, 0 and -2
+    x[0, 32] = 127 / 16
+    x[0, 33], x[0, 34], x[0, 35] = 2.5 / 16, 0.5 / 16, -1.5 / 16
+    q, d = O.quantize_q8_blocks(x)
+    assert d.tolist() == [[0.0, 1 / 16]]
+    assert q[0, :32].tolist() == [0] * 32
+    assert q[0, 32:36].tolist() == [127, 3, 1, -2]
+    assert O.dequantize_q8_blocks(q, d)[0, :32].tolist() == [0.0] * 32
+
+
+def test_q8_error_bound_extremes_and_idempotence():
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((50, 512)) * rng.uniform(0.01, 30, (50, 1))).astype(np.float32)
+    q, d = O.quantize_q8_blocks(x)
+    dq = O.dequantize_q8_blocks(q, d)
+    d64 = d.astype(np.float64).repeat(32, axis=1)
+    # every value within half a step of its code
+    assert np.all(np.abs(x - dq) <= d64 / 2 * (1 + 1e-6))
+    # the largest magnitude of every block takes code +-127
+    blocks = np.abs(x.reshape(50, 16, 32))
+    top = np.take_along_axis(q.reshape(50, 16, 32), blocks.argmax(axis=2)[..., None], axis=2)
+    assert np.all(np.abs(top.astype(int)) == 127)
+    # quantising the dequantised values gives back the same codes and scales
+    q2, d2 = O.quantize_q8_blocks(dq.astype(np.float32))
+    assert np.array_equal(q2, q) and np.array_equal(d2, d)
+
+
+def test_q8_cache_rows_keep_rope_and_exact_cache_attends_alike():
+    rng = np.random.default_rng(22)
+    d_c, d_hr, T = 64, 8, 20
+    # latent values on the exact grid of each block's scale (each block holds a 127)
+    codes = rng.integers(-127, 128, (T, d_c))
+    codes[:, ::32] = 127
+    rows = np.concatenate([codes * 2.0 ** -5, rng.standard_normal((T, d_hr))], axis=1)
+    q, d, k_r = O.quantize_cache_rows(rows, d_c)
+    assert np.array_equal(k_r, rows[:, d_c:])
+    back = O.dequantize_cache_rows(q, d, k_r)
+    assert np.array_equal(back, rows)
+    q_lat = rng.standard_normal((4, d_c + d_hr))
+    o1, l1 = O.attend_latent(q_lat, rows, d_c=d_c, d_h=16)
+    o2, l2 = O.attend_latent(q_lat, back, d_c=d_c, d_h=16)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
 def test_merge_partials_equals_whole():
     rng = np.random.default_rng(7)
     q_lat = rng.standard_normal((4, 20))
