@@ -36,7 +36,7 @@ METRIC = "MLA decode tokens/s and latent-cache GB/s (% of HBM/tensor roofline), 
 # DRAM bytes (read + write) of one decode_tc_kernel launch on this workload,
 # from the ncu capture summarised in profiles/decode_tc_kernel_b64_t4096.md;
 # valid only while the kernel sources hash to the captured ones.
-PROFILED_DECODE = {"sources": {"decode_tc.cu": "5e30b051ede633c3", "ptx.cuh": "1fd1dc657a7fe061"},
+PROFILED_DECODE = {"sources": {"decode_tc.cu": "661b9209bf3c159d", "ptx.cuh": "1fd1dc657a7fe061"},
                    "workload": (64, 4096), "traffic_bytes": 314375168}
 
 

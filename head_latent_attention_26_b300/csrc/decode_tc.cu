@@ -37,8 +37,11 @@
 //   busy pushing an 18-MMA score batch could not see that P is ready; with two
 //   issuers each kind goes in as soon as its inputs are.  S runs ahead of the
 //   softmax: while the row warps turn tile t into probabilities they hold
-//   S(t+1) in registers and the tensor pipe runs O(t-1) and S(t+2) (one TMEM
-//   buffer for S is enough).
+//   S(t+1) in registers and the tensor pipe runs O(t-1) and S(t+2).  S has a
+//   single TMEM buffer (O 256 + q~ 128 + q^R 16 + P 32 + S 64 = 496 of the 512
+//   columns), so S(t+2) waits for every row warp to have read S(t+1); on the
+//   B=64 x T=4096 workload a row warp waits about 490 of the tile's ~2600
+//   cycles for its next S.
 // * Rescaling of O is lazy: the running max only moves when a tile's max
 //   exceeds it by more than 2^8, which keeps every exp2 argument <= 8 and the
 //   result exact (numerator and denominator share the stale max).
