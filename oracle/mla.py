@@ -71,6 +71,7 @@ __all__ = [
     "mla_cache_elements",
     "decode_sequence",
     "decode_batch",
+    "prefill_expanded",
 ]
 
 
@@ -452,6 +453,42 @@ def decode_sequence(h_rows, h_query, t: int, W: dict, n_h: int, base: float = 10
         o_lat, lse_lat = attend_latent(q_lat, rows, c.shape[1], q_c.shape[1], heads=heads)
         res.update(q_lat=q_lat, rows=rows, o_lat=o_lat, lse_lat=lse_lat)
     return res
+
+
+def prefill_expanded(h, W: dict, n_h: int, base: float = 10000.0):
+    """Causal attention for every token of a prompt at once, in the expanded form.
+
+    [perforder] "極限最適化の代償：MLA特有の学習負荷と独自Tritonカーネルという障壁":
+    in the prefill phase many tokens are processed together and the
+    up-projection of the latent vector to full keys and values becomes a large
+    matrix product; [kasblo] "「キャッシュを減らせた」と「その割合だけ速い」は別の評価"
+    names the reference implementation's "naive" branch that keeps the
+    expanded K/V.  Row t of the prompt attends rows 0..t ([qiita] "Attention
+    計算").  All P queries of a head at once: S = (Q^C K^C^T + Q^R K^R^T) /
+    sqrt(d_h + d_h^R) over the P x P positions, entries with j > t set to -inf,
+    a row-wise softmax with its log-sum-exp, O = A V, then u = W^O [o].
+
+    h: [P, d].  Returns o [P, n_h, d_h], lse [P, n_h] and u [P, d].
+    """
+    h = f64(h)
+    P = h.shape[0]
+    pos = np.arange(P)
+    c, k_r = kv_latent(h, W["W_dkv"], W["W_kr"], pos, base)
+    _, q_c, q_r_raw = query_parts(h, W["W_dq"], W["W_uq"], W["W_qr"], n_h)
+    q_r = rope(q_r_raw, pos[:, None], base)
+    d_h, d_hr = q_c.shape[2], q_r.shape[2]
+    inv = 1.0 / math.sqrt(d_h + d_hr)
+    later = np.triu(np.ones((P, P), dtype=bool), 1)  # key j after query t
+    o = np.empty((P, n_h, d_h))
+    lse = np.empty((P, n_h))
+    for i in range(n_h):
+        k_c, v = expand_kv(c, W["W_uk"], W["W_uv"], i, d_h)
+        s = (q_c[:, i] @ k_c.T + q_r[:, i] @ k_r.T) * inv
+        s[later] = -np.inf
+        a, lse[:, i] = softmax_lse(s)
+        o[:, i] = a @ v
+    u = np.stack([output_projection(o[t], W["W_o"]) for t in range(P)])
+    return o, lse, u
 
 
 def decode_batch(q_lat, pool_rows, block_table, seq_lens, cu_q, block: int, d_c: int, d_h: int,

@@ -371,6 +371,55 @@ def test_q8_cache_rows_keep_rope_and_exact_cache_attends_alike():
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
+# --------------------------------------------------------------------------
+# Prefill: every prompt position at once (expanded form)
+# --------------------------------------------------------------------------
+
+def test_prefill_first_token_sees_only_itself():
+    W, rng = _random_layer(31)
+    h = rng.standard_normal((6, 32))
+    o, lse, _ = O.prefill_expanded(h, W, n_h=4)
+    c, k_r = O.kv_latent(h[:1], W["W_dkv"], W["W_kr"], [0])
+    _, q_c, q_r_raw = O.query_parts(h[:1], W["W_dq"], W["W_uq"], W["W_qr"], 4)
+    for i in range(4):
+        k_c, v = O.expand_kv(c, W["W_uk"], W["W_uv"], i, 8)
+        # one visible key: the output is its value, the lse its score
+        assert np.allclose(o[0, i], v[0], atol=1e-13)
+        s = (q_c[0, i] @ k_c[0] + q_r_raw[0, i] @ k_r[0]) / math.sqrt(12)  # position 0: no rotation
+        assert abs(lse[0, i] - s) < 1e-12
+
+
+def test_prefill_is_causal():
+    W, rng = _random_layer(32)
+    h = rng.standard_normal((7, 32))
+    o, lse, u = O.prefill_expanded(h, W, n_h=4)
+    h2 = h.copy()
+    h2[4] += 3.0  # a later token changes
+    o2, lse2, u2 = O.prefill_expanded(h2, W, n_h=4)
+    assert np.array_equal(o2[:4], o[:4]) and np.array_equal(lse2[:4], lse[:4]) and np.array_equal(u2[:4], u[:4])
+    assert not np.allclose(o2[4:], o[4:])
+
+
+def test_prefill_matches_per_token_decode_and_brute_force():
+    W, rng = _random_layer(33)
+    P = 9
+    h = rng.standard_normal((P, 32))
+    o, lse, u = O.prefill_expanded(h, W, n_h=4)
+    for t in range(P):
+        r = O.decode_sequence(h[:t + 1], h[t], t, W, n_h=4, with_latent=False)
+        assert np.max(np.abs(o[t] - r["o"])) <= 1e-12 * np.max(np.abs(r["o"]))
+        assert np.max(np.abs(lse[t] - r["lse"])) <= 1e-12 * max(1.0, np.max(np.abs(r["lse"])))
+        assert np.max(np.abs(u[t] - r["u"])) <= 1e-12 * np.max(np.abs(r["u"]))
+    # scalar loops on a tiny layer
+    n_h, d_h, d_hr, d_c, d_cq, d = 2, 2, 2, 3, 3, 4
+    Wt, rng = _random_layer(34, n_h, d_h, d_hr, d_c, d_cq, d)
+    ht = rng.standard_normal((4, d))
+    ot, _, ut = O.prefill_expanded(ht, Wt, n_h=n_h)
+    for t in range(4):
+        o_b, u_b = _brute_decode(ht.tolist(), t, {k: v.tolist() for k, v in Wt.items()}, n_h, d_h, d_hr)
+        assert np.allclose(ot[t].reshape(-1), o_b, atol=1e-12) and np.allclose(ut[t], u_b, atol=1e-12)
+
+
 def test_merge_partials_equals_whole():
     rng = np.random.default_rng(7)
     q_lat = rng.standard_normal((4, 20))

@@ -90,6 +90,28 @@ def _folded_weight_head_shift(orig):
     return bad
 
 
+def _prefill_mask_includes_next_key(orig):
+    # the causal mask lets row t see row t+1
+    def bad(h, W, n_h, base=10000.0):
+        h = M.f64(h)
+        P = h.shape[0]
+        pos = np.arange(P)
+        c, k_r = M.kv_latent(h, W["W_dkv"], W["W_kr"], pos, base)
+        _, q_c, q_r_raw = M.query_parts(h, W["W_dq"], W["W_uq"], W["W_qr"], n_h)
+        q_r = M.rope(q_r_raw, pos[:, None], base)
+        d_h, d_hr = q_c.shape[2], q_r.shape[2]
+        later = np.triu(np.ones((P, P), dtype=bool), 2)
+        o, lse = np.empty((P, n_h, d_h)), np.empty((P, n_h))
+        for i in range(n_h):
+            k_c, v = M.expand_kv(c, W["W_uk"], W["W_uv"], i, d_h)
+            s = (q_c[:, i] @ k_c.T + q_r[:, i] @ k_r.T) / np.sqrt(d_h + d_hr)
+            s[later] = -np.inf
+            a, lse[:, i] = M.softmax_lse(s)
+            o[:, i] = a @ v
+        return o, lse, np.stack([M.output_projection(o[t], W["W_o"]) for t in range(P)])
+    return bad
+
+
 MUTATIONS = [
     ("rope", _rope_wrong_sign),
     ("kv_latent", _kv_latent_position_off_by_one),
@@ -100,6 +122,7 @@ MUTATIONS = [
     ("merge_partials", _merge_equal_weights),
     ("quantize_q8_blocks", _q8_round_half_even),
     ("absorbed_query_weight", _folded_weight_head_shift),
+    ("prefill_expanded", _prefill_mask_includes_next_key),
 ]
 
 
