@@ -1,4 +1,4 @@
-"""Benchmark of one MLA decode step on B300 (see the design doc for the recipe).
+"""Benchmark of one MLA decode step on B300.
 
 Workload (default): DeepSeek-V2 attention layer (d=5120, n_h=128, d_h=128,
 d_h^R=64, d_c=512, d_c'=1536), batched decode B=64 sequences of T=4096 cached

@@ -53,7 +53,7 @@ extern "C" {
 typedef enum {
   MLA_OK = 0,
   MLA_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size, inconsistent dims */
-  MLA_ERR_UNSUPPORTED = 2,    /* valid request this build does not implement */
+  MLA_ERR_UNSUPPORTED = 2,    /* valid request the library does not implement */
   MLA_ERR_WORKSPACE = 3,      /* workspace pointer null or smaller than required */
   MLA_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
   MLA_ERR_DEVICE_TIMEOUT = 5, /* a bounded device-side wait ran out */

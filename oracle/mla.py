@@ -19,7 +19,7 @@ definition: K and V are expanded per head and per cached token.  The absorbed
 intermediates (latent query, latent output) are also written out, each from
 its own defining equation, for per-kernel parity.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 
 * RoPE: interleaved pairs (x[2k], x[2k+1]) rotated by angle pos * theta_k,
   theta_k = base ** (-2k / d_r); positions are 0-based.  The pages only say
