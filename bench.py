@@ -1,16 +1,27 @@
 """Benchmark of one MLA decode step on B300.
 
-Workload (default): DeepSeek-V2 attention layer (d=5120, n_h=128, d_h=128,
-d_h^R=64, d_c=512, d_c'=1536), batched decode B=64 sequences of T=4096 cached
-rows each, one new token per sequence, 64-row cache blocks scattered over a
-seeded random permutation of the pool.  One step = the whole path for the 64
-new tokens: query projection, cache append, W^UK absorption, latent attention
-(+ split combine), W^UV / W^O output.
+Workloads (DeepSeek-V2 attention layer: d=5120, n_h=128, d_h=128, d_h^R=64,
+d_c=512, d_c'=1536; 64-row cache blocks scattered over a seeded random
+permutation of the pool):
+
+  b64_t4096    (default) B=64 sequences x T=4096 cached rows, 1 new token each
+  b1_t4096     B=1, T=4096
+  b1_t131072   B=1, T=131072 (128K context), 1% of the cached rows scaled by 8
+  ragged_b128  B=128, T_b ~ U[512, 16384], 1 or 2 new tokens per sequence
+
+One step = the whole path for the step's new tokens: query projection, cache
+append, W^UK absorption, latent attention (+ split combine), W^UV / W^O output.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
 
-Prints one JSON line.  Under torchrun every rank runs an independent replica
-on its own GPU (the path has no exchange step); the time is the max over ranks.
+The timed steps are replayed as CUDA graphs of the library's C-ABI calls (the
+calls are captured once; a replay launches the same kernels with no host work
+in between), so the device time of the step is measured, not the host's
+launch rate.  Event nodes around each step's decode call give the decode time
+of every timed step.  Prints one JSON line.  Under torchrun every rank runs
+an independent replica on its own GPU (the path has no exchange step); the
+time is the max over ranks.
 """
 
 from __future__ import annotations
@@ -33,9 +44,9 @@ from head_latent_attention_26_b300 import synth  # noqa: E402
 
 METRIC = "MLA decode tokens/s and latent-cache GB/s (% of HBM/tensor roofline), 1×B300"
 
-# DRAM bytes (read + write) of one decode_tc_kernel launch on this workload,
-# from the ncu capture summarised in profiles/decode_tc_kernel_b64_t4096.md;
-# valid only while the kernel sources hash to the captured ones.
+# DRAM bytes (read + write) of one decode_tc_kernel launch on the B=64, T=4096
+# workload, from an ncu capture of the kernel sources with these hashes; the
+# figure is reported only while the sources still hash to them.
 PROFILED_DECODE = {"sources": {"decode_tc.cu": "661b9209bf3c159d", "ptx.cuh": "1fd1dc657a7fe061"},
                    "workload": (64, 4096), "traffic_bytes": 314375168}
 
@@ -50,8 +61,20 @@ def _profiled_traffic(B: int, T: int):
             if hashlib.sha256(f.read()).hexdigest()[:16] != digest:
                 return None
     return PROFILED_DECODE["traffic_bytes"]
-B_DEFAULT, T_DEFAULT = 64, 4096
+
+
 SEED = 1003
+B_DEFAULT, T_DEFAULT = 64, 4096
+# A timed region at least this long runs the GPU at its sustained (power
+# capped) tensor rate; shorter ones are compared with the burst rate.
+SUSTAINED_REGION_S = 1.0
+
+WORKLOADS = {
+    "b64_t4096": dict(kind="uniform", B=64, T=4096, hot=0.0),
+    "b1_t4096": dict(kind="uniform", B=1, T=4096, hot=0.0),
+    "b1_t131072": dict(kind="uniform", B=1, T=131072, hot=0.01),
+    "ragged_b128": dict(kind="ragged", B=128, lo=512, hi=16384, hot=0.0),
+}
 
 
 def _peaks():
@@ -101,6 +124,21 @@ def _job_rate(units_per_rank: int, ws: int, ms: float) -> float:
     return units_per_rank * ws / (ms * 1e-3)
 
 
+def roofline_choice(t_hbm_s: float, t_tc_burst_s: float, t_tc_sus_s: float, region_s: float):
+    """Which roof binds the decode kernel and the tensor peak it is held to.
+
+    The tensor peak is the burst one unless the timed region lasts seconds (a
+    kernel inside a long loop runs at the sustained, power-capped rate).  The
+    binding roof is the slower of HBM and tensor: the larger lower bound on
+    the kernel's time.  Returns (bound, t_roof_s, tensor_peak_kind)."""
+    sustained = region_s >= SUSTAINED_REGION_S
+    t_tc = t_tc_sus_s if sustained else t_tc_burst_s
+    kind = "sustained" if sustained else "burst"
+    if t_tc > t_hbm_s:
+        return "tensor", t_tc, kind
+    return "hbm", t_hbm_s, kind
+
+
 _SAMPLER = r"""
 import ctypes, sys, time
 lib = ctypes.CDLL("libnvidia-ml.so.1")
@@ -115,15 +153,16 @@ if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(c)) == 0:
     print("max", c.value, flush=True)
 while True:
     if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(c)) == 0 and get_r(h, ctypes.byref(r)) == 0:
-        print(c.value, r.value, flush=True)
-    time.sleep(0.005)
+        print(time.time(), c.value, r.value, flush=True)
+    time.sleep(0.002)
 """
 
 
 class ClockSampler:
-    """SM clock and throttle-reason samples every 5 ms while the timed region
-    runs, read through NVML (the library nvidia-smi uses) by a separate
-    process so the sampling does not compete with this process for the GIL."""
+    """SM clock and throttle-reason samples every 2 ms, read through NVML (the
+    library nvidia-smi uses) by a separate process so the sampling does not
+    compete with this process for the GIL.  Only samples taken while a timed
+    region ran count (mark() brackets each region)."""
 
     REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
                "sw_power_cap": 0x4}
@@ -133,6 +172,7 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self.thread = None
+        self.windows = []
 
     def _bus_id(self) -> str:
         props = torch.cuda.get_device_properties(self.dev)
@@ -153,9 +193,13 @@ class ClockSampler:
         self.thread.start()
         time.sleep(0.3)  # the sampler is up before the timed region starts
 
+    def mark(self, t0: float, t1: float):
+        self.windows.append((t0, t1))
+
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["sampler unavailable"], "samples": 0}
+        time.sleep(0.01)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -167,53 +211,93 @@ class ClockSampler:
             f = ln.split()
             if len(f) == 2 and f[0] == "max":
                 smax = float(f[1])
-            elif len(f) == 2:
-                sm.append(float(f[0]))
+            elif len(f) == 3:
+                t = float(f[0])
+                if self.windows and not any(a - 0.002 <= t <= b + 0.002 for a, b in self.windows):
+                    continue
+                sm.append(float(f[1]))
                 for name, bit in self.REASONS.items():
-                    if int(f[1]) & bit:
+                    if int(f[2]) & bit:
                         reasons.add(name)
         sm.sort()
         med = sm[len(sm) // 2] if sm else None
-        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm), "source": "nvml"}
+        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm),
+                "source": "nvml, samples inside the timed regions"}
 
 
 # ---------------------------------------------------------------------------
-# workload
+# workloads
 # ---------------------------------------------------------------------------
 
-def make_workload(B: int, T: int, device="cuda"):
-    """Weights, a pool holding T-1 prior rows per sequence, and the step's inputs."""
+def workload_shape(name: str, batch=None, seq_len=None):
+    """(lens, q_counts, hot_frac, description) of a named workload; --batch /
+    --seq-len override the sizes of the uniform ones."""
+    wl = WORKLOADS[name]
+    if wl["kind"] == "uniform":
+        B = batch if batch is not None else wl["B"]
+        T = seq_len if seq_len is not None else wl["T"]
+        desc = (f"MLA decode step, DeepSeek-V2 layer, B={B} sequences x T={T} cached rows, "
+                "64-row blocks in a permuted pool, 1 new token per sequence")
+        if wl["hot"]:
+            desc += f", {wl['hot']:.0%} of cached rows scaled by 8"
+        return [T] * B, [1] * B, wl["hot"], desc
+    B = wl["B"]
+    lens = synth.ragged_lengths(B, wl["lo"], wl["hi"], SEED).tolist()
+    qc = synth.query_counts(B, SEED).tolist()
+    desc = (f"MLA decode step, DeepSeek-V2 layer, ragged batch B={B}, T_b ~ U[{wl['lo']}, {wl['hi']}] "
+            f"(sum {sum(lens)} rows), 1 or 2 new tokens per sequence ({sum(qc)} tokens), "
+            "new rows appended by mla_cache_append inside the step")
+    return lens, qc, wl["hot"], desc
+
+
+def make_workload(lens, qc, hot: float, device="cuda"):
+    """Weights, a pool holding each sequence's prior rows (T_b - q_b of them),
+    and the step's inputs (q_b new tokens per sequence at the last positions)."""
     d = synth.V2
     W = synth.weights(d, SEED, device=device)
     W_dkr = torch.cat([W["W_dkv"], W["W_kr"]], dim=0).contiguous()
-    lens = [T] * B
+    B = len(lens)
     table, n_blocks = synth.block_table(lens, d.block, SEED)
     table = table.to(device)
     pool = torch.empty(n_blocks, d.block, d.width, dtype=torch.bfloat16, device=device)
     flat = pool.view(-1, d.width)
-    # prior rows: c ~ N(0,1), k^R ~ N(0,1), the distribution W^DKV h and RoPE(W^KR h)
-    # have for h ~ N(0,1), W ~ N(0, 1/fan_in)
-    for b0 in range(0, B, 8):
-        nb = min(8, B - b0)
-        rows = synth.normal((nb * T, d.width), SEED + b0, "prior_rows", device=device)
-        j = torch.arange(T, device=device)
-        for k in range(nb):
-            slots = table[b0 + k][j // d.block].long() * d.block + (j % d.block)
-            flat[slots] = rows[k * T:(k + 1) * T]
-        del rows
-    x = synth.hidden(B, d, SEED, name="h_new", device=device)
+    # prior rows: c ~ N(0,1), k^R ~ N(0,1), the distribution W^DKV h and
+    # RoPE(W^KR h) have for h ~ N(0,1), W ~ N(0, 1/fan_in)
+    for b in range(B):
+        n_prior = int(lens[b]) - int(qc[b])
+        for j0 in range(0, n_prior, 65536):
+            j1 = min(n_prior, j0 + 65536)
+            rows = synth.normal((j1 - j0, d.width), SEED + b, f"prior_rows_{j0}", device=device)
+            j = torch.arange(j0, j1, device=device)
+            slots = table[b][j // d.block].long() * d.block + (j % d.block)
+            flat[slots] = rows
+    if hot:
+        # a seeded share of each sequence's prior rows scaled by 8 (exact in bf16)
+        for b in range(B):
+            n_prior = int(lens[b]) - int(qc[b])
+            j = synth.pick_rows(n_prior, hot, SEED + b).to(device)
+            slots = table[b][j // d.block].long() * d.block + (j % d.block)
+            flat[slots] *= 8
+    n_tok = int(sum(qc))
+    x = synth.hidden(n_tok, d, SEED, name="h_new", device=device)
+    seq_idx, pos = [], []
+    for b in range(B):
+        for k in range(int(qc[b])):
+            seq_idx.append(b)
+            pos.append(int(lens[b]) - int(qc[b]) + k)
     inp = {
         "x": x,
-        "seq_idx": torch.arange(B, dtype=torch.int32, device=device),
-        "pos": torch.full((B,), T - 1, dtype=torch.int32, device=device),
-        "seq_lens": torch.full((B,), T, dtype=torch.int32, device=device),
-        "cu_q": torch.arange(B + 1, dtype=torch.int32, device=device),
+        "seq_idx": torch.tensor(seq_idx, dtype=torch.int32, device=device),
+        "pos": torch.tensor(pos, dtype=torch.int32, device=device),
+        "seq_lens": torch.tensor([int(t) for t in lens], dtype=torch.int32, device=device),
+        "cu_q": synth.cu_from_counts(qc).to(device),
     }
     return d, W, W_dkr, table, pool, inp
 
 
 def algorithmic(B: int, T: int, d=synth.V2):
-    """Bytes and flops the decode kernel must move / do (one launch)."""
+    """Bytes and flops the decode kernel must move / do for B sequences of T
+    rows with one query token each (one launch)."""
     cache = B * T * d.width * 2
     q = B * d.n_h * d.width * 2
     out = B * d.n_h * d.d_c * 2 + B * d.n_h * 4
@@ -221,9 +305,43 @@ def algorithmic(B: int, T: int, d=synth.V2):
     return cache, cache + q + out, flops
 
 
+def algorithmic_tokens(visible, d=synth.V2):
+    """The same for query tokens that see `visible[n]` cached rows each: per
+    token its rows of cache, its latent query read, its o_lat / lse written."""
+    rows = int(sum(visible))
+    n = len(visible)
+    cache = rows * d.width * 2
+    total = cache + n * d.n_h * d.width * 2 + n * d.n_h * d.d_c * 2 + n * d.n_h * 4
+    flops = d.n_h * rows * (2 * d.width + 2 * d.d_c)
+    return cache, total, flops
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+
+def _capture(step, n_steps: int, events: bool):
+    """A CUDA graph of n_steps calls of step(); with events, a pair of timing
+    event nodes around each step's decode call (returned in order)."""
+    g = torch.cuda.CUDAGraph()
+    pairs = []
+    with torch.cuda.graph(g):
+        for _ in range(n_steps):
+            step(pairs if events else None)
+    return g, pairs
+
+
+def _capture_chunks(step, K: int, events: bool, chunk: int = 256):
+    graphs, pairs = [], []
+    done = 0
+    while done < K:
+        n = min(chunk, K - done)
+        g, p = _capture(step, n, events)
+        graphs.append(g)
+        pairs.extend(p)
+        done += n
+    return graphs, pairs
+
 
 def run_ours(args):
     ws, rank = _dist()
@@ -233,132 +351,156 @@ def run_ours(args):
     from head_latent_attention_26_b300 import build
     build.build()
     from head_latent_attention_26_b300 import mla
-    B, T = args.batch, args.seq_len
-    d, W, W_dkr, table, pool, inp = make_workload(B, T)
-    m = mla.MLA(d, T + 64, torch.bfloat16)
+    lens, qc, hot, desc = workload_shape(args.workload, args.batch, args.seq_len)
+    d, W, W_dkr, table, pool, inp = make_workload(lens, qc, hot)
+    B, N = len(lens), int(sum(qc))
+    m = mla.MLA(d, max(lens) + 64, torch.bfloat16)
     assert m.tensor_path
     bufs = {
-        "q_c": torch.empty(B, d.n_h, d.d_h, dtype=torch.bfloat16, device="cuda"),
-        "q_r": torch.empty(B, d.n_h, d.d_hr, dtype=torch.bfloat16, device="cuda"),
-        "q_lat": torch.empty(B, d.n_h, d.width, dtype=torch.bfloat16, device="cuda"),
-        "o_lat": torch.empty(B, d.n_h, d.d_c, dtype=torch.bfloat16, device="cuda"),
-        "lse": torch.empty(B, d.n_h, dtype=torch.float32, device="cuda"),
-        "u": torch.empty(B, d.d_model, dtype=torch.bfloat16, device="cuda"),
+        "q_c": torch.empty(N, d.n_h, d.d_h, dtype=torch.bfloat16, device="cuda"),
+        "q_r": torch.empty(N, d.n_h, d.d_hr, dtype=torch.bfloat16, device="cuda"),
+        "q_lat": torch.empty(N, d.n_h, d.width, dtype=torch.bfloat16, device="cuda"),
+        "o_lat": torch.empty(N, d.n_h, d.d_c, dtype=torch.bfloat16, device="cuda"),
+        "lse": torch.empty(N, d.n_h, dtype=torch.float32, device="cuda"),
+        "u": torch.empty(N, d.d_model, dtype=torch.bfloat16, device="cuda"),
     }
-    ws_dec = m.workspace("decode", m.decode_workspace_bytes(B, args.num_workers))
-    dec_ev = []
+    ws_dec = m.workspace("decode", m.decode_workspace_bytes(N, args.num_workers))
+    x_dev = torch.empty_like(inp["x"])
+    x_dev.copy_(inp["x"])
 
-    def step(x, time_decode=False):
+    def step(pairs=None, x=None):
+        x = x_dev if x is None else x
+        if pairs is not None:
+            ea = torch.cuda.Event(enable_timing=True, external=True)
+            ea.record()
         m.q_proj(x, W["W_dq"], W["W_uq"], W["W_qr"], bufs["q_c"], bufs["q_r"])
         m.cache_append(x, W_dkr, inp["seq_idx"], inp["pos"], table, pool)
+        if pairs is not None:
+            eb = torch.cuda.Event(enable_timing=True, external=True)
+            eb.record()
         m.absorb_q(bufs["q_c"], bufs["q_r"], inp["pos"], W["W_uk"], bufs["q_lat"])
-        if time_decode:
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if pairs is not None:
+            e0 = torch.cuda.Event(enable_timing=True, external=True)
             e0.record()
         m.decode(bufs["q_lat"], pool, table, inp["seq_lens"], inp["cu_q"], args.num_workers, bufs["o_lat"],
                  bufs["lse"], ws_dec)
-        if time_decode:
+        if pairs is not None:
+            e1 = torch.cuda.Event(enable_timing=True, external=True)
             e1.record()
-            dec_ev.append((e0, e1))
+            pairs.append((ea, eb, e0, e1))
         m.out(bufs["o_lat"], W["W_uv"], W["W_o"], bufs["u"])
 
-    for _ in range(args.warmup):
-        step(inp["x"])
+    # eager calls first: the library sets kernel attributes, encodes tensor
+    # maps and sizes its launches once; the captured calls then do no host work
+    step()
+    torch.cuda.synchronize()
     m.check()
-
-    def barrier():
-        _barrier(ws)
+    warm, _ = _capture(step, max(3, args.warmup), events=False)
+    graphs, pairs = _capture_chunks(step, args.steps, events=True)
+    for _ in range(2):
+        warm.replay()
+    torch.cuda.synchronize()
+    m.check()
 
     clocks = ClockSampler(local)
     clocks.start()
-    barrier()
+    _barrier(ws)
+    w0 = time.time()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
-    for _ in range(args.steps):
-        step(inp["x"], time_decode=True)
+    for g in graphs:
+        g.replay()
     t1.record()
-    barrier()
-    clk = clocks.stop()
+    _barrier(ws)
+    clocks.mark(w0, time.time())
     m.check()
     ms = t0.elapsed_time(t1) / args.steps
-    dec_ms = sum(a.elapsed_time(b) for a, b in dec_ev) / len(dec_ev)
-    launches_per_step = 2 + 1 + 1 + 3 + 2  # q_proj (W^DQ; W^UQ and W^QR fused), append, absorb, plan+decode+combine, out
+    # per timed step: the q_proj + append part, and the decode call (plan +
+    # decode + combine), each between event nodes on the step's stream
+    app_ms = sum(ea.elapsed_time(eb) for ea, eb, _, _ in pairs) / len(pairs)
+    dec_ms = sum(e0.elapsed_time(e1) for _, _, e0, e1 in pairs) / len(pairs)
+    region_s = ms * args.steps * 1e-3
 
-    # end to end through the public API with host buffers: H2D of the step's
-    # inputs, the step, D2H of u -- all inside the timed region
+    # the same steps without event nodes (nothing between the kernels but the
+    # stream order): the step time the timing nodes do not perturb
+    graphs_plain, _ = _capture_chunks(step, args.steps, events=False)
+    _barrier(ws)
+    w0 = time.time()
+    t0.record()
+    for g in graphs_plain:
+        g.replay()
+    t1.record()
+    _barrier(ws)
+    clocks.mark(w0, time.time())
+    ms_plain = t0.elapsed_time(t1) / args.steps
+    del graphs_plain
+
+    # end to end through the public API with host buffers: every step copies
+    # its inputs from pinned host memory, runs, and copies u back -- all inside
+    # the timed region (one graph replay per step, launched from the host loop)
     h_x = inp["x"].cpu().pin_memory()
     h_pos = inp["pos"].cpu().pin_memory()
     h_lens = inp["seq_lens"].cpu().pin_memory()
-    h_u = torch.empty(B, d.d_model, dtype=torch.bfloat16).pin_memory()
-    x_dev = torch.empty_like(inp["x"])
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
+    h_u = torch.empty(N, d.d_model, dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step(_=None):
         x_dev.copy_(h_x, non_blocking=True)
         inp["pos"].copy_(h_pos, non_blocking=True)
         inp["seq_lens"].copy_(h_lens, non_blocking=True)
-        step(x_dev)
+        step()
         h_u.copy_(bufs["u"], non_blocking=True)
-    e1.record()
-    barrier()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
+
+    g_e2e, _ = _capture(e2e_step, 1, events=False)
+    for _ in range(3):
+        g_e2e.replay()
+    _barrier(ws)
+    w0 = time.time()
+    t0.record()
+    for _ in range(args.steps):
+        g_e2e.replay()
+    t1.record()
+    _barrier(ws)
+    clocks.mark(w0, time.time())
+    e2e_ms = t0.elapsed_time(t1) / args.steps
+    clk = clocks.stop()
     m.check()
+    # kernels per step: q_proj 2 (W^DQ; W^UQ with W^QR), append 1, absorb 1,
+    # decode 3 (plan, attention, combine), out 2 (W^UV, W^O)
+    n_launch = 9
+    del graphs, warm, g_e2e
 
-    # the two routes to the latent query for the same tokens: runtime
-    # absorption (q_proj + absorb_q, the step above) and the folded weight
-    # W^UK_i^T W^UQ_i formed once ahead of time (q_proj_absorbed)
-    W_abs = m.absorb_weights(W["W_uq"], W["W_uk"])
-    q_lat_f = torch.empty_like(bufs["q_lat"])
-    n_q = max(3, min(args.steps, 300))
-
-    def time_route(fn):
-        for _ in range(3):
-            fn()
-        barrier()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(n_q):
-            fn()
-        b.record()
-        barrier()
-        return a.elapsed_time(b) / n_q
-
-    def runtime_route():
-        m.q_proj(inp["x"], W["W_dq"], W["W_uq"], W["W_qr"], bufs["q_c"], bufs["q_r"])
-        m.absorb_q(bufs["q_c"], bufs["q_r"], inp["pos"], W["W_uk"], bufs["q_lat"])
-
-    rt_ms = time_route(runtime_route)
-    fold_ms = time_route(lambda: m.q_proj_absorbed(inp["x"], W["W_dq"], W_abs, W["W_qr"], inp["pos"], q_lat_f))
-    m.check()
-    del W_abs
-    ms, dec_ms, e2e_ms, rt_ms, fold_ms = _max_over_ranks([ms, dec_ms, e2e_ms, rt_ms, fold_ms], ws)
+    ms, ms_plain, dec_ms, app_ms, e2e_ms = _max_over_ranks([ms, ms_plain, dec_ms, app_ms, e2e_ms], ws)
     if rank != 0:
         return None
 
     hbm, tf_burst, tf_sus, src = _peaks()
-    cache_b, dec_bytes, flops = algorithmic(B, T, d)
+    visible = []
+    for b in range(B):
+        for k in range(int(qc[b])):
+            visible.append(int(lens[b]) - int(qc[b]) + k + 1)
+    cache_b, dec_bytes, flops = algorithmic_tokens(visible, d)
     t = dec_ms * 1e-3
     gbs = dec_bytes / t / 1e9
     tflops = flops / t / 1e12
-    # binding roofline of the decode kernel: the slower of HBM and tensor at the
-    # measured peaks (sustained tensor peak: the kernel runs inside a long loop)
-    t_hbm, t_tc = dec_bytes / (hbm * 1e9), flops / (tf_sus * 1e12)
-    if t_tc >= t_hbm:
-        roof = {"bound": "tensor", "achieved": round(tflops, 1), "peak": tf_sus, "unit": "TFLOP/s",
-                "frac": round(tflops / tf_sus, 4)}
+    t_hbm = dec_bytes / (hbm * 1e9)
+    bound, t_roof, tc_kind = roofline_choice(t_hbm, flops / (tf_burst * 1e12), flops / (tf_sus * 1e12), region_s)
+    tf_peak = tf_sus if tc_kind == "sustained" else tf_burst
+    if bound == "tensor":
+        roof = {"bound": "tensor", "achieved": round(tflops, 1), "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": round(tflops / tf_peak, 4)}
     else:
         roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4)}
-    roof.update(kernel="decode_tc_kernel (+plan, combine)", peak_source=f"{src} (MEASURED_PEAKS.json)",
-                traffic=args.traffic if args.traffic is not None else _profiled_traffic(B, T), other={"hbm": {"achieved_gbs": round(gbs, 1), "peak": hbm,
-                                                     "frac": round(gbs / hbm, 4)},
-                                             "tensor": {"achieved_tflops": round(tflops, 1),
-                                                        "peak_sustained": tf_sus, "peak_burst": tf_burst,
-                                                        "frac_sustained": round(tflops / tf_sus, 4),
-                                                        "frac_burst": round(tflops / tf_burst, 4)}},
+    traffic = args.traffic if args.traffic is not None else _profiled_traffic(B, lens[0] if len(set(lens)) == 1 else -1)
+    roof.update(kernel="decode_tc_kernel (+plan, combine)", peak_source=f"{src} (MEASURED_PEAKS.json), "
+                f"tensor peak {tc_kind} (timed region {region_s * 1e3:.1f} ms)",
+                traffic=traffic,
+                other={"hbm": {"achieved_gbs": round(gbs, 1), "peak": hbm, "frac": round(gbs / hbm, 4)},
+                       "tensor": {"achieved_tflops": round(tflops, 1), "peak_sustained": tf_sus,
+                                  "peak_burst": tf_burst, "frac_sustained": round(tflops / tf_sus, 4),
+                                  "frac_burst": round(tflops / tf_burst, 4)}},
                 algorithmic_bytes=dec_bytes, algorithmic_flops=flops, decode_us=round(dec_ms * 1e3, 2))
     n = ws
-    value = _job_rate(B, n, ms)
+    value = _job_rate(N, n, ms)
     res = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -372,28 +514,32 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"MLA decode step, DeepSeek-V2 layer, B={B} sequences x T={T} cached rows, "
-                               "64-row blocks in a permuted pool, 1 new token per sequence",
-                   "batch": B, "seq_len": T, "num_workers": args.num_workers,
+        "config": {"workload": desc, "batch": B, "tokens_per_step": N,
+                   "seq_len": lens[0] if len(set(lens)) == 1 else f"U[{min(lens)}, {max(lens)}]",
+                   "cached_rows": int(sum(lens)), "num_workers": args.num_workers,
                    "parallelism": f"replicas x{n}" if n > 1 else "single GPU",
-                   "l2": "no flush: the step reads > L2 (302 MB cache + 300 MB weights)"},
+                   "l2": f"no flush: every step streams {(298_024_960 + cache_b) / 1e6:.0f} MB of weights and "
+                         "cache, more than the 126 MB L2",
+                   "timing": "K steps captured as CUDA graphs of the C-ABI calls and replayed; events around "
+                             "each step's decode call inside the graphs"},
+        "ms_per_step_without_event_nodes": round(ms_plain, 4),
         "latent_cache_gbs": round(cache_b / t / 1e9, 1),
-        "decode_tokens_per_s": round(_job_rate(B, n, dec_ms), 1),
+        "decode_tokens_per_s": round(_job_rate(N, n, dec_ms), 1),
+        "q_proj_append_us": round(app_ms * 1e3, 2),
         "roofline": roof,
-        "e2e": {"value": round(_job_rate(B, n, e2e_ms), 1), "unit": "tokens/s",
+        "e2e": {"value": round(_job_rate(N, n, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h_x.numel() * 2 + h_pos.numel() * 4 + h_lens.numel() * 4,
                 "d2h_bytes_per_step": h_u.numel() * 2},
-        "query_routes": {"runtime_absorb_us": round(rt_ms * 1e3, 2), "folded_weight_us": round(fold_ms * 1e3, 2),
-                         "weight_bytes": {"runtime": 2 * d.d_cq * (d.d_model + d.n_h * (d.d_h + d.d_hr))
-                                          + 2 * d.n_h * d.d_h * d.d_c,
-                                          "folded": 2 * d.d_cq * (d.d_model + d.n_h * (d.d_c + d.d_hr))},
-                         "note": "W^DQ, W^UQ + W^QR, W^UK absorb (runtime) vs W^DQ, folded W^UK_i^T W^UQ_i + W^QR "
-                                 f"(one launch), {n_q} back-to-back calls each, outside the timed step"},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": n_launch * args.steps,
         "clocks": clk,
     }
+    if WORKLOADS[args.workload]["kind"] == "ragged":
+        # the pool's valid rows: every sequence's T_b rows, (d_c + d_hr) bf16 values each
+        res["cache_bytes"] = {"valid": int(sum(lens)) * d.width * 2,
+                              "formula": "(d_c + d_hr) * sum(T) * 2",
+                              "pool_bytes": pool.numel() * 2}
     if not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(B, T, budget_s=args.cpu_budget)
+        res["cpu_baseline"] = cpu_baseline(lens, qc, args.workload, budget_s=args.cpu_budget)
     return res
 
 
@@ -412,23 +558,26 @@ def _oracle_inputs(B: int):
 
 
 def _prior_rows(B: int, T: int, b: int):
+    """T - 1 prior rows of sequence b (the recipe of make_workload)."""
     d = synth.V2
-    b0 = (b // 8) * 8
-    g = synth.normal((min(8, B - b0) * T, d.width), SEED + b0, "prior_rows", device="cpu")
-    return g[(b - b0) * T:(b - b0 + 1) * T]
+    parts = [synth.normal((min(T - 1, j0 + 65536) - j0, d.width), SEED + b, f"prior_rows_{j0}", device="cpu")
+             for j0 in range(0, max(T - 1, 1), 65536)]
+    return torch.cat(parts)[:T - 1]
 
 
 def _oracle_token(Wn, x, rows_bf16, T: int, b: int):
-    """The oracle, as it stands, for token b of the workload: its cache row,
-    query, expanded K/V over the sequence's T rows, softmax, W^O.  Returns u."""
+    """The oracle, as it stands, for one new token at position T - 1 after
+    T - 1 cached rows: its cache row, query, expanded K/V over the T rows,
+    softmax, W^O.  Returns u."""
     import numpy as np
     import oracle as O
     d = synth.V2
     rows = O.f64(rows_bf16)
-    c_new, kr_new = O.kv_latent(O.f64(x[b:b + 1]), Wn["W_dkv"], Wn["W_kr"], [T - 1], d.rope_base)
+    xb = O.f64(x[b % x.shape[0]:b % x.shape[0] + 1])
+    c_new, kr_new = O.kv_latent(xb, Wn["W_dkv"], Wn["W_kr"], [T - 1], d.rope_base)
     c = np.concatenate([rows[:T - 1, :d.d_c], c_new])
     k_r = np.concatenate([rows[:T - 1, d.d_c:], kr_new])
-    _, q_c, q_r_raw = O.query_parts(O.f64(x[b:b + 1]), Wn["W_dq"], Wn["W_uq"], Wn["W_qr"], d.n_h)
+    _, q_c, q_r_raw = O.query_parts(xb, Wn["W_dq"], Wn["W_uq"], Wn["W_qr"], d.n_h)
     o, _ = O.attend_expanded(q_c[0], O.rope(q_r_raw[0], T - 1, d.rope_base), c, k_r, Wn["W_uk"], Wn["W_uv"])
     return O.output_projection(o, Wn["W_o"])
 
@@ -442,20 +591,31 @@ def _blas_threads():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(B: int, T: int, budget_s: float = 15.0):
+def _token_list(lens, qc):
+    """(sequence, visible rows) of every query token, in token order."""
+    out = []
+    for b, (L, q) in enumerate(zip(lens, qc)):
+        for k in range(int(q)):
+            out.append((b, int(L) - int(q) + k + 1))
+    return out
+
+
+def cpu_baseline(lens, qc, workload: str, budget_s: float = 15.0):
     """Time the fp64 oracle on whole tokens of the workload until budget_s of
     oracle arithmetic has run (input generation is outside the timer)."""
     t_start = time.perf_counter()
-    Wn, x = _oracle_inputs(B)
+    toks = _token_list(lens, qc)
+    Wn, x = _oracle_inputs(len(toks))
     done, elapsed = 0, 0.0
-    while done < B and (done == 0 or elapsed < budget_s):
-        rows = _prior_rows(B, T, done)
+    while done < len(toks) and (done == 0 or elapsed < budget_s):
+        b, T = toks[done]
+        rows = _prior_rows(len(lens), T, b)
         t0 = time.perf_counter()
         _oracle_token(Wn, x, rows, T, done)
         elapsed += time.perf_counter() - t0
         done += 1
     return {"value": round(done / elapsed, 4), "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
-            "sample": f"{done} of {B} tokens of the B={B}, T={T} workload (expanded K/V, fp64 numpy), "
+            "sample": f"{done} of {len(toks)} tokens of the {workload} workload (expanded K/V, fp64 numpy), "
                       f"{elapsed:.1f} s of oracle time; input generation untimed",
             "wall_s": round(time.perf_counter() - t_start, 1)}
 
@@ -464,11 +624,14 @@ def run_reference(args):
     ws, rank = _dist()
     if rank != 0:
         return None
-    B, T = args.batch, args.seq_len
+    lens, qc, _, desc = workload_shape(args.workload, args.batch, args.seq_len)
+    toks = _token_list(lens, qc)
+    B = len(toks)
     Wn, x = _oracle_inputs(B)
     total_s = 0.0
     for s in range(args.warmup + args.steps):
-        rows = _prior_rows(B, T, s % B)
+        b, T = toks[s % B]
+        rows = _prior_rows(len(lens), T, b)
         t0 = time.perf_counter()
         _oracle_token(Wn, x, rows, T, s % B)
         if s >= args.warmup:
@@ -488,11 +651,10 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"MLA decode step, DeepSeek-V2 layer, B={B} sequences x T={T} cached rows, "
-                               "64-row blocks in a permuted pool, 1 new token per sequence",
-                   "batch": B, "seq_len": T},
+        "config": {"workload": desc, "batch": len(lens), "tokens_per_step": B,
+                   "seq_len": lens[0] if len(set(lens)) == 1 else f"U[{min(lens)}, {max(lens)}]"},
         "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
-                         "sample": f"each step = 1 of the B={B} tokens through the fp64 oracle "
+                         "sample": f"each step = 1 of the {B} tokens of the workload through the fp64 oracle "
                                    "(expanded K/V); input generation untimed"},
         "e2e": {"value": round(v, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -501,17 +663,20 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--batch", type=int, default=B_DEFAULT)
-    ap.add_argument("--seq-len", type=int, default=T_DEFAULT)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="b64_t4096")
+    ap.add_argument("--batch", type=int, default=None, help="override B of a uniform workload")
+    ap.add_argument("--seq-len", type=int, default=None, help="override T of a uniform workload")
     ap.add_argument("--num-workers", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per decode launch from an ncu capture of this kernel version")
     args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         res = run_reference(args)
     else:

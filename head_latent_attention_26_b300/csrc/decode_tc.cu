@@ -904,26 +904,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const int* __restrict__ pr
   if (lane == 0) lse[static_cast<size_t>(n) * kHeads + h] = L;
 }
 
-bool encode_pool_map(CUtensorMap* m, const void* pool, long long rows, uint32_t box_cols, CUtensorMapSwizzle sw) {
-  auto enc = tma_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kWidth), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kWidth) * 2};
-  cuuint32_t box[2] = {box_cols, static_cast<cuuint32_t>(kTile)};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+bool encode_pool_maps(const mla_handle* h, Maps* maps, const void* pool, long long rows) {
+  return tensor_map_2d(h, &maps->latent, pool, kWidth, rows, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         tensor_map_2d(h, &maps->rope, pool, kWidth, rows, 32, kTile, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // plan -> decode -> combine, each allowed to launch while its predecessor finishes.
-cudaError_t launch_decode_kernels(const Maps& maps, const Params& prm, int W, int n_tok, const int* seq_lens,
-                                  const int* cu_q, int batch, int max_blocks, float* lse, int* status, cudaStream_t s) {
+cudaError_t launch_decode_kernels(const mla_handle* h, const Maps& maps, const Params& prm, int W, int n_tok,
+                                  const int* seq_lens, const int* cu_q, int batch, int max_blocks, float* lse,
+                                  int* status, cudaStream_t s) {
   cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s, 1, seq_lens, cu_q, batch, n_tok, max_blocks, W,
                              const_cast<int*>(prm.prefix), const_cast<int2*>(prm.tok_info),
                              const_cast<int*>(prm.worker_plan), const_cast<int*>(prm.plan_flags), status);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  e = kernel_attrs_once(h, reinterpret_cast<const void*>(decode_tc_kernel), kSmemBytes, false);
   if (e != cudaSuccess) return e;
   e = launch_pdl(decode_tc_kernel, dim3(2 * W), dim3(kThreads), kSmemBytes, s, 1, maps, prm);
   if (e != cudaSuccess) return e;
@@ -978,9 +972,7 @@ cudaError_t launch_decode_tc(const mla_handle* h, const void* q_lat, const void*
   const int W = resolve_workers(h, num_workers);
   Maps maps;
   const long long rows = static_cast<long long>(n_pool_blocks) * kBlockRows;
-  if (!encode_pool_map(&maps.latent, pool, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_pool_map(&maps.rope, pool, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B))
-    return cudaErrorInvalidValue;
+  if (!encode_pool_maps(h, &maps, pool, rows)) return cudaErrorInvalidValue;
   Params prm;
   set_workspace(prm, static_cast<uint8_t*>(ws), ws_layout(static_cast<size_t>(n_tok), static_cast<size_t>(W)));
   prm.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
@@ -998,7 +990,7 @@ cudaError_t launch_decode_tc(const mla_handle* h, const void* q_lat, const void*
   prm.workers = W;
   prm.scale_log2 = h->dims.scale * kLog2e;
 
-  return launch_decode_kernels(maps, prm, W, n_tok, seq_lens, cu_q, batch, max_blocks, lse, h->status, s);
+  return launch_decode_kernels(h, maps, prm, W, n_tok, seq_lens, cu_q, batch, max_blocks, lse, h->status, s);
 }
 
 
@@ -1050,9 +1042,15 @@ constexpr size_t kNoAllocScratchBytes = kNoAllocLayout.total;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-void* g_noalloc_ptr[kMaxDevices] = {};
 }  // namespace
+
+cudaError_t decode_noalloc_scratch_address(void** ptr) {
+  // the array's host-side name stands in for it; its device address on the
+  // current device comes from the runtime
+  *ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(ptr, g_noalloc_scratch);
+  return e == cudaSuccess && *ptr == nullptr ? cudaErrorInvalidSymbol : e;
+}
 
 size_t decode_noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
 int decode_noalloc_max_tokens() { return kNoAllocMaxTokens; }
@@ -1064,22 +1062,13 @@ int launch_decode_tc_noalloc(const mla_handle* h, const void* q_lat, const void*
                              int batch, int n_tok, int num_workers, void* o_lat, float* lse, cudaStream_t s) {
   const int W = num_workers > 0 ? num_workers : min(max(1, h->num_sms / 2), kNoAllocMaxWorkers);
   if (n_tok > kNoAllocMaxTokens || W > kNoAllocMaxWorkers) return 1;
-  // Once per device, with that device current: the device address of the
-  // scratch array (its host-side name is only a stand-in for it).
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 2;
-  if (!g_noalloc_ptr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return 2;
-    g_noalloc_ptr[dev] = ptr;
-  }
+  // the handle looked up the array's device address when it was created
+  if (!h->noalloc_scratch) return 2;
   Maps maps;
   const long long rows = static_cast<long long>(n_pool_blocks) * kBlockRows;
-  if (!encode_pool_map(&maps.latent, pool, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_pool_map(&maps.rope, pool, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B))
-    return 2;
+  if (!encode_pool_maps(h, &maps, pool, rows)) return 2;
   Params prm;
-  set_workspace(prm, static_cast<uint8_t*>(g_noalloc_ptr[dev]), kNoAllocLayout);
+  set_workspace(prm, static_cast<uint8_t*>(h->noalloc_scratch), kNoAllocLayout);
   prm.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
   prm.block_table = block_table;
   prm.seq_lens = seq_lens;
@@ -1094,7 +1083,7 @@ int launch_decode_tc_noalloc(const mla_handle* h, const void* q_lat, const void*
   prm.n_pool_blocks = n_pool_blocks;
   prm.workers = W;
   prm.scale_log2 = h->dims.scale * kLog2e;
-  return launch_decode_kernels(maps, prm, W, n_tok, seq_lens, cu_q, batch, max_blocks, lse, h->status, s) ==
+  return launch_decode_kernels(h, maps, prm, W, n_tok, seq_lens, cu_q, batch, max_blocks, lse, h->status, s) ==
                  cudaSuccess
              ? 0
              : 2;

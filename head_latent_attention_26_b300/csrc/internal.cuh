@@ -8,9 +8,35 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <unordered_map>
+#include <unordered_set>
 #include <utility>
 
 #include "mla.h"
+
+namespace mla {
+// What a 2-D tiled tensor map encodes: the same key always gives the same map,
+// so a handle encodes each one once and reuses it on later calls.
+struct MapKey {
+  const void* base;
+  long long cols, rows;
+  int box_cols, box_rows, swizzle, dtype;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && cols == o.cols && rows == o.rows && box_cols == o.box_cols &&
+           box_rows == o.box_rows && swizzle == o.swizzle && dtype == o.dtype;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    size_t h = std::hash<const void*>()(k.base);
+    for (long long v : {k.cols, k.rows, static_cast<long long>(k.box_cols), static_cast<long long>(k.box_rows),
+                        static_cast<long long>(k.swizzle), static_cast<long long>(k.dtype)})
+      h = h * 1000003u ^ std::hash<long long>()(v);
+    return h;
+  }
+};
+}  // namespace mla
 
 struct mla_handle {
   mla_dims dims;
@@ -23,6 +49,14 @@ struct mla_handle {
   long long wait_limit;
   bool tensor_path;  // tcgen05 decode serves these dims
   bool proj_tc;      // tcgen05 projection kernels serve these dims
+  // Device address of the decode's fixed scratch array on this handle's
+  // device (looked up in mla_create with the device current), or null.
+  void* noalloc_scratch;
+  // Host-side launch state kept across calls so that a call does no repeated
+  // driver work: encoded tensor maps and the kernels whose attributes are set.
+  mutable std::mutex mu;
+  mutable std::unordered_map<mla::MapKey, CUtensorMap, mla::MapKeyHash> maps;
+  mutable std::unordered_set<const void*> attrs_set;
 };
 
 namespace mla {
@@ -124,6 +158,17 @@ cudaError_t launch_decode_tc(const mla_handle* h, const void* q_lat, const void*
                              cudaStream_t s);
 // cuTensorMapEncodeTiled from the driver (looked up once); null if unavailable.
 PFN_cuTensorMapEncodeTiled_v12000 tma_encoder();
+// A 2-D tiled tensor map of a row-major [rows, cols] tensor with boxes of
+// box_cols x box_rows, 16-bit (bf16) or 8-bit (u8) elements, encoded once per
+// handle and key and copied out of the handle's cache afterwards.
+bool tensor_map_2d(const mla_handle* h, CUtensorMap* out, const void* base, long long cols, long long rows,
+                   int box_cols, int box_rows, CUtensorMapSwizzle sw,
+                   CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+// Sets a kernel's dynamic shared-memory size (and, when asked, the
+// non-portable cluster-size opt-in) the first time this handle launches it.
+cudaError_t kernel_attrs_once(const mla_handle* h, const void* fn, int smem_bytes, bool nonportable_cluster);
+// Device address of the decode's fixed scratch array for the current device.
+cudaError_t decode_noalloc_scratch_address(void** ptr);
 // tcgen05 projections (bf16, d_h = 128, widths multiples of 64)
 cudaError_t launch_linear_tc(const mla_handle* h, const void* X, int x_cols, const void* W, int in, int out,
                              int groups, int x_group_cols, void* Y, long long ldy, int n_tok, cudaStream_t s);

@@ -45,6 +45,48 @@ bool proj_tc_dims(const mla_dims* d) {
 
 }  // namespace
 
+namespace mla {
+
+bool tensor_map_2d(const mla_handle* h, CUtensorMap* out, const void* base, long long cols, long long rows,
+                   int box_cols, int box_rows, CUtensorMapSwizzle sw, CUtensorMapDataType dt) {
+  const int eb = dt == CU_TENSOR_MAP_DATA_TYPE_UINT8 ? 1 : 2;
+  const MapKey key{base, cols, rows, box_cols, box_rows, static_cast<int>(sw), static_cast<int>(dt)};
+  std::lock_guard<std::mutex> lock(h->mu);
+  auto it = h->maps.find(key);
+  if (it != h->maps.end()) {
+    *out = it->second;
+    return true;
+  }
+  auto enc = tma_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * eb};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[2] = {1, 1};
+  CUtensorMap m;
+  if (enc(&m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  // a serving loop reuses a handful of buffers; a caller that keeps handing
+  // new ones only ever pays for one encode per call
+  if (h->maps.size() >= 1024) h->maps.clear();
+  h->maps.emplace(key, m);
+  *out = m;
+  return true;
+}
+
+cudaError_t kernel_attrs_once(const mla_handle* h, const void* fn, int smem_bytes, bool nonportable_cluster) {
+  std::lock_guard<std::mutex> lock(h->mu);
+  if (h->attrs_set.count(fn)) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e == cudaSuccess && nonportable_cluster)
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) h->attrs_set.insert(fn);
+  return e;
+}
+
+}  // namespace mla
+
 extern "C" {
 
 const char* mla_status_string(mla_status s) {
@@ -93,6 +135,11 @@ mla_status mla_create(const mla_dims* dims, int max_pos, mla_handle** out) {
             cudaMemcpy(h->rope_cos, c.data(), n * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemcpy(h->rope_sin, s.data(), n * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemset(h->status, 0, sizeof(int)) == cudaSuccess;
+  // The fixed scratch of mla_decode_noalloc: its device address on this
+  // device, looked up now with the device current.  The lookup also loads the
+  // library's device code here, so the array is reserved at creation rather
+  // than at the first decode call.
+  if (ok && h->tensor_path) ok = mla::decode_noalloc_scratch_address(&h->noalloc_scratch) == cudaSuccess;
   if (!ok) {
     mla_destroy(h);
     return MLA_ERR_CUDA;

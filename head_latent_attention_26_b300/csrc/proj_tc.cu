@@ -421,16 +421,13 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
 }
 
 template <int NT, int STAGES, int MODE, int MT>
-cudaError_t launch_proj_nt(const ProjMaps& maps, const ProjParams& p, int nsplit, int tile_groups, int n_tiles,
-                           cudaStream_t s) {
+cudaError_t launch_proj_nt(const mla_handle* h, const ProjMaps& maps, const ProjParams& p, int nsplit,
+                           int tile_groups, int n_tiles, cudaStream_t s) {
   constexpr size_t kSmem = STAGES * (kABytes + NT * kBK * 2) + sizeof(ProjShared<STAGES, NT>) + 1024;
   auto kern = proj_kernel<NT, STAGES, MODE, MT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
+  // both attributes once per handle (the cluster opt-in is harmless for small splits)
+  cudaError_t e = kernel_attrs_once(h, reinterpret_cast<const void*>(kern), static_cast<int>(kSmem), true);
   if (e != cudaSuccess) return e;
-  if (nsplit > 8) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
   // The largest split (cluster size) not above nsplit whose clusters can all
   // be resident at once: clusters are placed within one GPC, so a split that
   // fits the SM count can still leave a second wave.  Per device and cluster
@@ -472,15 +469,15 @@ cudaError_t launch_proj_nt(const ProjMaps& maps, const ProjParams& p, int nsplit
 // flight to reach its share of HBM bandwidth); larger grids run two CTAs per
 // SM with four.
 template <int MODE, int MT>
-cudaError_t launch_proj(const ProjMaps& maps, const ProjParams& p, int nsplit, int o_tiles, int num_sms,
+cudaError_t launch_proj(const mla_handle* h, const ProjMaps& maps, const ProjParams& p, int nsplit, int o_tiles,
                         cudaStream_t s) {
   const int groups = o_tiles / MT;
   if (p.n_tok <= 64) {
-    if (groups <= num_sms) return launch_proj_nt<64, 8, MODE, MT>(maps, p, nsplit, groups, 1, s);
-    return launch_proj_nt<64, 4, MODE, MT>(maps, p, nsplit, groups, 1, s);
+    if (groups <= h->num_sms) return launch_proj_nt<64, 8, MODE, MT>(h, maps, p, nsplit, groups, 1, s);
+    return launch_proj_nt<64, 4, MODE, MT>(h, maps, p, nsplit, groups, 1, s);
   }
-  if (p.n_tok <= 128) return launch_proj_nt<128, 4, MODE, MT>(maps, p, nsplit, groups, 1, s);
-  return launch_proj_nt<256, 3, MODE, (MT > 2 ? 2 : MT)>(maps, p, nsplit, o_tiles / (MT > 2 ? 2 : MT),
+  if (p.n_tok <= 128) return launch_proj_nt<128, 4, MODE, MT>(h, maps, p, nsplit, groups, 1, s);
+  return launch_proj_nt<256, 3, MODE, (MT > 2 ? 2 : MT)>(h, maps, p, nsplit, o_tiles / (MT > 2 ? 2 : MT),
                                                         (p.n_tok + 255) / 256, s);
 }
 
@@ -512,16 +509,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tma_encoder() {
   return fn;
 }
 
-bool encode_bf16_2d(CUtensorMap* m, const void* base, long long cols, long long rows, int box_cols, int box_rows) {
-  auto enc = tma_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+// bf16 [rows, cols] with 128B-swizzled boxes, through the handle's map cache
+bool encode_bf16_2d(const mla_handle* h, CUtensorMap* m, const void* base, long long cols, long long rows,
+                    int box_cols, int box_rows) {
+  return tensor_map_2d(h, m, base, cols, rows, box_cols, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 namespace {
@@ -547,7 +538,7 @@ cudaError_t launch_linear_tc(const mla_handle* h, const void* X, int x_cols, con
                              int groups, int x_group_cols, void* Y, long long ldy, int n_tok, cudaStream_t s) {
   ProjMaps maps;
   const int nt = token_tile(n_tok);
-  if (!encode_bf16_2d(&maps.w, W, in, out, kBK, kBM) || !encode_bf16_2d(&maps.x, X, x_cols, n_tok, kBK, nt))
+  if (!encode_bf16_2d(h, &maps.w, W, in, out, kBK, kBM) || !encode_bf16_2d(h, &maps.x, X, x_cols, n_tok, kBK, nt))
     return cudaErrorInvalidValue;
   maps.w2 = maps.w;
   ProjParams p = base_params(h, n_tok);
@@ -559,7 +550,7 @@ cudaError_t launch_linear_tc(const mla_handle* h, const void* X, int x_cols, con
   p.y = static_cast<__nv_bfloat16*>(Y);
   p.ldy = ldy;
   p.seg1_tiles = 1 << 30;
-  return launch_proj<kModeLinear, 1>(maps, p, pick_split(h, o_tiles, n_tok, p.k_blocks), o_tiles, h->num_sms, s);
+  return launch_proj<kModeLinear, 1>(h, maps, p, pick_split(h, o_tiles, n_tok, p.k_blocks), o_tiles, s);
 }
 
 cudaError_t launch_linear2_tc(const mla_handle* h, const void* X, int in, const void* W1, int out1, void* Y1,
@@ -567,8 +558,8 @@ cudaError_t launch_linear2_tc(const mla_handle* h, const void* X, int in, const 
                               cudaStream_t s) {
   ProjMaps maps;
   const int nt = token_tile(n_tok);
-  if (!encode_bf16_2d(&maps.w, W1, in, out1, kBK, kBM) || !encode_bf16_2d(&maps.w2, W2, in, out2, kBK, kBM) ||
-      !encode_bf16_2d(&maps.x, X, in, n_tok, kBK, nt))
+  if (!encode_bf16_2d(h, &maps.w, W1, in, out1, kBK, kBM) || !encode_bf16_2d(h, &maps.w2, W2, in, out2, kBK, kBM) ||
+      !encode_bf16_2d(h, &maps.x, X, in, n_tok, kBK, nt))
     return cudaErrorInvalidValue;
   ProjParams p = base_params(h, n_tok);
   const int t1 = (out1 + kBM - 1) / kBM, t2 = (out2 + kBM - 1) / kBM;
@@ -580,7 +571,7 @@ cudaError_t launch_linear2_tc(const mla_handle* h, const void* X, int in, const 
   p.y2 = static_cast<__nv_bfloat16*>(Y2);
   p.ldy2 = ldy2;
   p.seg1_tiles = t1;
-  return launch_proj<kModeLinear, 1>(maps, p, pick_split(h, t1 + t2, n_tok, p.k_blocks), t1 + t2, h->num_sms, s);
+  return launch_proj<kModeLinear, 1>(h, maps, p, pick_split(h, t1 + t2, n_tok, p.k_blocks), t1 + t2, s);
 }
 
 cudaError_t launch_q_absorbed_tc(const mla_handle* h, const void* c_q, const void* w_abs, const void* w_qr,
@@ -588,8 +579,8 @@ cudaError_t launch_q_absorbed_tc(const mla_handle* h, const void* c_q, const voi
   const mla_dims& d = h->dims;
   const int out1 = d.n_h * d.d_c, out2 = d.n_h * d.d_hr;
   ProjMaps maps;
-  if (!encode_bf16_2d(&maps.w, w_abs, d.d_cq, out1, kBK, kBM) || !encode_bf16_2d(&maps.w2, w_qr, d.d_cq, out2, kBK, kBM) ||
-      !encode_bf16_2d(&maps.x, c_q, d.d_cq, n_tok, kBK, token_tile(n_tok)))
+  if (!encode_bf16_2d(h, &maps.w, w_abs, d.d_cq, out1, kBK, kBM) || !encode_bf16_2d(h, &maps.w2, w_qr, d.d_cq, out2, kBK, kBM) ||
+      !encode_bf16_2d(h, &maps.x, c_q, d.d_cq, n_tok, kBK, token_tile(n_tok)))
     return cudaErrorInvalidValue;
   ProjParams p = base_params(h, n_tok);
   const int t1 = (out1 + kBM - 1) / kBM, t2 = (out2 + kBM - 1) / kBM;
@@ -599,7 +590,7 @@ cudaError_t launch_q_absorbed_tc(const mla_handle* h, const void* c_q, const voi
   p.seg1_tiles = t1;
   p.pos = pos;
   p.q_lat = static_cast<__nv_bfloat16*>(q_lat);
-  return launch_proj<kModeQFolded, 1>(maps, p, pick_split(h, t1 + t2, n_tok, p.k_blocks), t1 + t2, h->num_sms, s);
+  return launch_proj<kModeQFolded, 1>(h, maps, p, pick_split(h, t1 + t2, n_tok, p.k_blocks), t1 + t2, s);
 }
 
 cudaError_t launch_cache_append_tc(const mla_handle* h, const void* x, const void* w_dkr, const int* seq_idx,
@@ -608,8 +599,8 @@ cudaError_t launch_cache_append_tc(const mla_handle* h, const void* x, const voi
   const mla_dims& d = h->dims;
   const int width = d.d_c + d.d_hr;
   ProjMaps maps;
-  if (!encode_bf16_2d(&maps.w, w_dkr, d.d_model, width, kBK, kBM) ||
-      !encode_bf16_2d(&maps.x, x, d.d_model, n_new, kBK, token_tile(n_new)))
+  if (!encode_bf16_2d(h, &maps.w, w_dkr, d.d_model, width, kBK, kBM) ||
+      !encode_bf16_2d(h, &maps.x, x, d.d_model, n_new, kBK, token_tile(n_new)))
     return cudaErrorInvalidValue;
   ProjParams p = base_params(h, n_new);
   const int o_tiles = (width + kBM - 1) / kBM;
@@ -624,7 +615,7 @@ cudaError_t launch_cache_append_tc(const mla_handle* h, const void* x, const voi
   p.pool = static_cast<__nv_bfloat16*>(pool);
   maps.w2 = maps.w;
   p.seg1_tiles = 1 << 30;
-  return launch_proj<kModeAppend, 1>(maps, p, pick_split(h, o_tiles, n_new, p.k_blocks), o_tiles, h->num_sms, s);
+  return launch_proj<kModeAppend, 1>(h, maps, p, pick_split(h, o_tiles, n_new, p.k_blocks), o_tiles, s);
 }
 
 cudaError_t launch_absorb_q_tc(const mla_handle* h, const void* q_c, const void* q_r, const int* pos, int n_tok,
@@ -632,8 +623,8 @@ cudaError_t launch_absorb_q_tc(const mla_handle* h, const void* q_c, const void*
   const mla_dims& d = h->dims;
   ProjMaps maps;
   // W^UK as [n_h*d_h rows, d_c columns]; boxes of 64 rows x 64 latent columns
-  if (!encode_bf16_2d(&maps.w, w_uk, d.d_c, static_cast<long long>(d.n_h) * d.d_h, 64, kBK) ||
-      !encode_bf16_2d(&maps.x, q_c, static_cast<long long>(d.n_h) * d.d_h, n_tok, kBK, token_tile(n_tok)))
+  if (!encode_bf16_2d(h, &maps.w, w_uk, d.d_c, static_cast<long long>(d.n_h) * d.d_h, 64, kBK) ||
+      !encode_bf16_2d(h, &maps.x, q_c, static_cast<long long>(d.n_h) * d.d_h, n_tok, kBK, token_tile(n_tok)))
     return cudaErrorInvalidValue;
   ProjParams p = base_params(h, n_tok);
   const int per_head = (d.d_c + kBM - 1) / kBM;
@@ -652,12 +643,12 @@ cudaError_t launch_absorb_q_tc(const mla_handle* h, const void* q_c, const void*
   // tiles stream in one wave and the epilogue and the RoPE items are spread
   // over four CTAs per head.  At 64 tokens this takes 9.8 us against 17.6 us
   // for one eight-stage CTA per head (back-to-back calls, weights not in L2).
-  if (n_tok <= 64) return launch_proj_nt<64, 2, kModeAbsorb, 1>(maps, p, 1, per_head * d.n_h, 1, s);
+  if (n_tok <= 64) return launch_proj_nt<64, 2, kModeAbsorb, 1>(h, maps, p, 1, per_head * d.n_h, 1, s);
   // more tokens: all of a head's output tiles in one CTA (they share the q^C tile)
   constexpr int kMT = 4;
   if (per_head % kMT != 0) return cudaErrorInvalidValue;
   // d_h = 128 is two k blocks: no split, so no cluster reduction
-  return launch_proj<kModeAbsorb, kMT>(maps, p, 1, per_head * d.n_h, h->num_sms, s);
+  return launch_proj<kModeAbsorb, kMT>(h, maps, p, 1, per_head * d.n_h, s);
 }
 
 }  // namespace mla

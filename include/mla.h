@@ -194,18 +194,21 @@ mla_status mla_decode(mla_handle* h, const void* q_lat, const void* pool, int n_
  * because that call can synchronise the device and take unbounded time.
  *
  * Its split-KV scratch is one fixed array in device memory (16,909,312 bytes
- * on the tensor path), created when the library is loaded and kept by every
- * device that loads it until the process exits.  Limits: n_tok <= 8192 and
- * at most 32 workers (num_workers = 0 picks min(SMs/2, 32)); larger requests
- * return MLA_ERR_WORKSPACE without launching.  Layer sizes outside the tensor
- * path need no scratch and run the generic kernels.
+ * on the tensor path) that every device holding the library keeps until the
+ * process exits.  It is reserved on a device when the first handle with the
+ * tensor-path sizes is created there: mla_create looks up the array's device
+ * address with that device current (which loads the library's device code
+ * there) and keeps it in the handle, so a caller that must not allocate later
+ * creates its handles before it hands the rest of the memory away.  Limits:
+ * n_tok <= 8192 and at most 32 workers (num_workers = 0 picks
+ * min(SMs/2, 32)); larger requests return MLA_ERR_WORKSPACE without
+ * launching.  Layer sizes outside the tensor path need no scratch and run the
+ * generic kernels.
  *
- * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  Every
- * call shares the one array: calls whose kernels overlap on the GPU (other
- * streams, other threads, other handles of the same device) race on it and
- * must be serialised by the caller.  Nothing in the array needs to start at
- * zero; each call writes every scratch byte it later reads.
+ * Every call shares the one array: calls whose kernels overlap on the GPU
+ * (other streams, other threads, other handles of the same device) race on
+ * it and must be serialised by the caller.  Nothing in the array needs to
+ * start at zero; each call writes every scratch byte it later reads.
  * This call allocates nothing and frees nothing.  Arguments and outputs are
  * those of mla_decode. */
 mla_status mla_decode_noalloc(mla_handle* h, const void* q_lat, const void* pool, int n_pool_blocks,

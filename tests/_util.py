@@ -14,6 +14,17 @@ OUT_TOL = 1e-2
 LSE_TOL = 2e-3
 
 
+# worst error seen per test case, printed at the end of the session so that
+# each configuration's margin against the gates is on record
+MARGINS: dict = {}
+
+
+def record(case: str, out_err: float = None, lse_err_: float = None):
+    """Keep the largest output / lse error seen for `case`."""
+    o, l = MARGINS.get(case, (0.0, 0.0))
+    MARGINS[case] = (max(o, out_err or 0.0), max(l, lse_err_ or 0.0))
+
+
 def row_rel_err(gpu, ref) -> float:
     """Largest per-row max|gpu-ref| / max|ref| over the leading axes."""
     g = np.asarray(gpu, dtype=np.float64)

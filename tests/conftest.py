@@ -8,3 +8,15 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA device (B300, sm_103a)")
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Print every case's worst output and lse error next to its gate."""
+    from _util import LSE_TOL, MARGINS, OUT_TOL
+    if not MARGINS:
+        return
+    tr = terminalreporter
+    tr.write_sep("-", "parity margins (worst error per case; gates: out %.0e, lse %.0e)" % (OUT_TOL, LSE_TOL))
+    for case in sorted(MARGINS):
+        o, l = MARGINS[case]
+        tr.write_line(f"{case:58s} out {o:.3e} ({o / OUT_TOL:5.1%} of gate)   lse {l:.3e} ({l / LSE_TOL:5.1%})")

@@ -14,7 +14,7 @@ import torch
 
 import oracle as O
 from head_latent_attention_26_b300 import build, synth
-from _util import LSE_TOL, OUT_TOL, batch_meta, latent_inputs, lse_err, row_rel_err, scatter_rows, to_np
+from _util import LSE_TOL, OUT_TOL, batch_meta, latent_inputs, lse_err, record, row_rel_err, scatter_rows, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -168,7 +168,7 @@ def _decode_case(v2, seq_lens, q_counts, seed, workers, spare=2, scale_rows=None
     return q_lat, per_seq, table, cu_q, o_lat, lse
 
 
-def _check_tokens(d, q_lat, per_seq, seq_lens, q_counts, o_lat, lse, tokens=None, heads=None):
+def _check_tokens(d, q_lat, per_seq, seq_lens, q_counts, o_lat, lse, tokens=None, heads=None, case=None):
     qn = None
     cu = np.concatenate([[0], np.cumsum(q_counts)])
     for b, L in enumerate(seq_lens):
@@ -185,6 +185,8 @@ def _check_tokens(d, q_lat, per_seq, seq_lens, q_counts, o_lat, lse, tokens=None
             o_ref, l_ref = O.attend_latent(q, rows_b[:t + 1], d.d_c, d.d_h, heads=hs)
             e_o = row_rel_err(to_np(o_lat[n])[hs], o_ref)
             e_l = lse_err(to_np(lse[n])[hs], l_ref)
+            if case:
+                record(case, e_o, e_l)
             assert e_o < OUT_TOL and e_l < LSE_TOL, (b, n, t, e_o, e_l)
 
 
@@ -202,7 +204,7 @@ def _check_tokens(d, q_lat, per_seq, seq_lens, q_counts, o_lat, lse, tokens=None
 ])
 def test_v2_decode_tensor_path(v2, seq_lens, q_counts, workers):
     q_lat, per_seq, _, _, o_lat, lse = _decode_case(v2, seq_lens, q_counts, 1005 + sum(seq_lens), workers)
-    _check_tokens(V2, q_lat, per_seq, seq_lens, q_counts, o_lat, lse)
+    _check_tokens(V2, q_lat, per_seq, seq_lens, q_counts, o_lat, lse, case="decode small cases")
 
 
 def test_v2_decode_split_matches_unsplit(v2):
@@ -211,7 +213,7 @@ def test_v2_decode_split_matches_unsplit(v2):
     for w in (1, 2, 5, 74, 150):
         q_lat, per_seq, _, _, o_lat, lse = _decode_case(v2, seq_lens, q_counts, 1006, w)
         results[w] = (to_np(o_lat), to_np(lse))
-    _check_tokens(V2, q_lat, per_seq, seq_lens, q_counts, o_lat, lse)
+    _check_tokens(V2, q_lat, per_seq, seq_lens, q_counts, o_lat, lse, case="decode split 1..150 workers")
     base_o, base_l = results[1]
     for w, (o, l) in results.items():
         assert row_rel_err(o, base_o) < OUT_TOL and lse_err(l, base_l) < LSE_TOL, w
@@ -233,11 +235,12 @@ def test_v2_layer_end_to_end(v2):
                        out=out)
     v2.check()
     ref = O.decode_sequence(to_np(h), to_np(h)[T - 1], T - 1, _np_weights(W), n_h=d.n_h, base=d.rope_base)
-    assert row_rel_err(to_np(out["q_c"])[0], ref["q_c"]) < OUT_TOL
-    assert row_rel_err(to_np(out["q_lat"])[0], ref["q_lat"]) < OUT_TOL
-    assert row_rel_err(to_np(out["o_lat"])[0], ref["o_lat"]) < OUT_TOL
-    assert lse_err(to_np(out["lse"])[0], ref["lse"]) < LSE_TOL
-    assert row_rel_err(to_np(u)[0], ref["u"]) < OUT_TOL
+    errs = {k: row_rel_err(to_np(out[k])[0], ref[k]) for k in ("q_c", "q_lat", "o_lat")}
+    errs["u"] = row_rel_err(to_np(u)[0], ref["u"])
+    e_l = lse_err(to_np(out["lse"])[0], ref["lse"])
+    for k, e in errs.items():
+        record(f"T=200 layer from h: {k}", e, e_l if k == "o_lat" else None)
+    assert all(e < OUT_TOL for e in errs.values()) and e_l < LSE_TOL, (errs, e_l)
 
 
 # ---------------------------------------------------------------------------
@@ -260,17 +263,20 @@ def test_v2_config_b1_t4096_end_to_end(v2):
                        out=out)
     v2.check()
     ref = O.decode_sequence(to_np(h), to_np(h)[T - 1], T - 1, _np_weights(W), n_h=d.n_h, base=d.rope_base)
-    assert row_rel_err(to_np(out["o_lat"])[0], ref["o_lat"]) < OUT_TOL
-    assert lse_err(to_np(out["lse"])[0], ref["lse"]) < LSE_TOL
-    assert row_rel_err(to_np(u)[0], ref["u"]) < OUT_TOL
+    e_o, e_l = row_rel_err(to_np(out["o_lat"])[0], ref["o_lat"]), lse_err(to_np(out["lse"])[0], ref["lse"])
+    e_u = row_rel_err(to_np(u)[0], ref["u"])
+    record("B=1 T=4096 layer from h: o_lat / lse", e_o, e_l)
+    record("B=1 T=4096 layer from h: u", e_u)
+    assert e_o < OUT_TOL and e_l < LSE_TOL and e_u < OUT_TOL
 
 
-def test_v2_config_b64_t4096_sampled(v2):
-    """B=64, T=4096, permuted pool: 5 sampled sequences, all heads."""
+def test_v2_config_b64_t4096_all_tokens(v2):
+    """B=64, T=4096, permuted pool, the bench's launch configuration: every
+    token, every head."""
     B, T = 64, 4096
     seq_lens, q_counts = [T] * B, [1] * B
     q_lat, per_seq, _, _, o_lat, lse = _decode_case(v2, seq_lens, q_counts, 1009, 0)
-    _check_tokens(V2, q_lat, per_seq, seq_lens, q_counts, o_lat, lse, tokens={0, 17, 31, 50, 63})
+    _check_tokens(V2, q_lat, per_seq, seq_lens, q_counts, o_lat, lse, case="B=64 T=4096 decode (64 tokens)")
 
 
 def test_v2_config_b1_t131072_hot_rows(v2):
@@ -278,43 +284,69 @@ def test_v2_config_b1_t131072_hot_rows(v2):
     T = 131072
     hot = synth.pick_rows(T, 0.01, 1010)
     q_lat, per_seq, _, _, o_lat, lse = _decode_case(v2, [T], [1], 1010, 0, scale_rows=hot)
-    _check_tokens(V2, q_lat, per_seq, [T], [1], o_lat, lse)
+    _check_tokens(V2, q_lat, per_seq, [T], [1], o_lat, lse, case="B=1 T=131072 hot rows decode")
 
 
-def test_v2_config_ragged_b128_sampled(v2):
+def test_v2_config_ragged_b128(v2):
     """B=128, lengths U[512,16384], 1 or 2 queries each; the newest rows are
-    appended by mla_cache_append in the same run.  Checks the valid cache
-    bytes against (d_c + d_hr) * sum(T) * 2 and 6 sampled tokens."""
+    appended by mla_cache_append in the same run into a pool whose every other
+    row holds a sentinel bit pattern.  Counts the cache bytes the pool holds
+    after the append against (d_c + d_hr) * sum(T) * 2, checks that the append
+    wrote exactly the new tokens' rows, and checks 48 sampled tokens plus every
+    token of the first eight sequences against the oracle."""
     d, B = V2, 128
     seed = 1011
     lens = synth.ragged_lengths(B, 512, 16384, seed).tolist()
     qc = synth.query_counts(B, seed).tolist()
-    table, n_blocks, cu_q, seq_lens, pos = batch_meta(lens, qc, d.block, seed)
+    table, n_blocks, cu_q, seq_lens, pos = batch_meta(lens, qc, d.block, seed, spare_blocks=3)
     n_tok = sum(qc)
-    assert sum(lens) * d.width * 2 == O.latent_cache_bytes(1, sum(lens), 1, d.d_c, d.d_hr, 2)
     q_lat, rows = latent_inputs(d, n_tok, sum(lens), seed)
     per_seq = list(torch.split(rows, lens))
-    pool = scatter_rows(per_seq, table, n_blocks, d.block, d.width)
-    # overwrite the newest q_len rows of every sequence through mla_cache_append
+    # prior rows (all but each sequence's newest q_len) placed by the test;
+    # everything else keeps the sentinel
+    sentinel = 0x3F3F
+    prior = [r[:L - q] for r, L, q in zip(per_seq, lens, qc)]
+    pool = scatter_rows(prior, table, n_blocks, d.block, d.width)
+    flat = pool.view(-1, d.width)
+    written = torch.zeros(flat.shape[0], dtype=torch.bool, device="cuda")
+    for b, r in enumerate(prior):
+        j = torch.arange(r.shape[0], device="cuda")
+        written[table[b][j // d.block].long() * d.block + (j % d.block)] = True
+    flat.view(torch.int16)[~written] = sentinel
+    before = flat.view(torch.int16).clone()
     W = synth.weights(d, seed, device="cuda")
     x = synth.hidden(n_tok, d, seed, device="cuda")
     seq_idx = torch.tensor(sum([[b] * q for b, q in enumerate(qc)], []), dtype=torch.int32, device="cuda")
     v2.cache_append(x, _w_dkr(W), seq_idx, pos, table, pool)
     o_lat, lse = v2.decode(q_lat, pool, table, seq_lens, cu_q)
     v2.check()
+    after = flat.view(torch.int16)
+    holds = (after != sentinel).any(dim=1)
+    # the cache the pool holds: every sequence's T_b rows of d_c + d_hr bf16 values
+    assert int(holds.sum()) * d.width * 2 == O.latent_cache_bytes(1, sum(lens), 1, d.d_c, d.d_hr, 2)
+    # the append changed exactly the new tokens' rows, at the oracle's slots
+    changed = torch.nonzero((after != before).any(dim=1)).flatten().cpu().tolist()
+    tab = table.cpu()
+    slots = [O.cache_slot(tab, int(b), int(p), d.block) for b, p in zip(seq_idx.tolist(), pos.tolist())]
+    assert sorted(changed) == sorted(slots)
     c, k_r = O.kv_latent(to_np(x), to_np(W["W_dkv"]), to_np(W["W_kr"]), to_np(pos), d.rope_base)
     new_rows = np.concatenate([c, k_r], axis=1)
+    e_rows = row_rel_err(to_np(flat[slots]), new_rows)
+    record("ragged B=128 appended rows", e_rows)
+    assert e_rows < OUT_TOL
     cu = np.concatenate([[0], np.cumsum(qc)])
     rng = np.random.default_rng(seed)
-    for n in sorted(rng.choice(n_tok, 6, replace=False).tolist()):
+    picks = set(rng.choice(n_tok, 48, replace=False).tolist()) | set(range(int(cu[8])))
+    for n in sorted(picks):
         b = int(np.searchsorted(cu, n, side="right") - 1)
         L = lens[b]
         t = L - (int(cu[b + 1]) - n)
         rows_b = to_np(per_seq[b])
         rows_b[L - qc[b]:] = new_rows[int(cu[b]):int(cu[b + 1])]
         o_ref, l_ref = O.attend_latent(to_np(q_lat[n]), rows_b[:t + 1], d.d_c, d.d_h)
-        assert row_rel_err(to_np(o_lat[n]), o_ref) < OUT_TOL, n
-        assert lse_err(to_np(lse[n]), l_ref) < LSE_TOL, n
+        e_o, e_l = row_rel_err(to_np(o_lat[n]), o_ref), lse_err(to_np(lse[n]), l_ref)
+        record("ragged B=128 decode (%d tokens)" % len(picks), e_o, e_l)
+        assert e_o < OUT_TOL and e_l < LSE_TOL, (n, e_o, e_l)
 
 
 # ---------------------------------------------------------------------------
