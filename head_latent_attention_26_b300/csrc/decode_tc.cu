@@ -144,54 +144,62 @@ struct Bars {
 static_assert(sizeof(Bars) <= 1024, "barrier block");
 constexpr uint32_t kBarSlot = kRowWarps * sizeof(uint64_t);  // stride of one slot of xin_full / inbox_free
 
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Params& p, Bars* bs,
+// A bounded wait ran out (or another role's did): records the timeout, with
+// the wait's site and tile the first time, and raises the CTA's abort flag.
+// Sites: producer 1 stage free, 2 RoPE slot free; score issuer 3 query
+// loaded, 4 stage landed, 5 S read by every row warp; value issuer 6 P
+// written by every row warp; exchange warp 7 partial block written, 8 peer
+// inbox slot free, 9 peer consumed the last blocks; row warps 10 outbox free,
+// 12 S ready, 13 peer partial scores landed, 14 previous O MMA done, 16
+// outbox free (epilogue), 17 last O MMA done (epilogue).
+__device__ __forceinline__ bool timed_out(long long i, const Params& p, Bars* bs, int site) {
+  if (i >= p.wait_limit || *reinterpret_cast<volatile int*>(&bs->abort)) {
+    if (i >= p.wait_limit) report_site(p.status, site, -1);
+    else report(p.status, MLA_ERR_DEVICE_TIMEOUT);
+    atomicExch(&bs->abort, 1);
+    return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Params& p, Bars* bs, int site,
                                          bool cluster_scope = false) {
   // an already completed phase is seen by the cheaper non-blocking test
   if (cluster_scope ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity)) return true;
   for (long long i = 0;; ++i) {
     if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    if (i >= p.wait_limit || *reinterpret_cast<volatile int*>(&bs->abort)) {
-      report(p.status, MLA_ERR_DEVICE_TIMEOUT);
-      atomicExch(&bs->abort, 1);
-      return false;
-    }
+    if (timed_out(i, p, bs, site)) return false;
   }
 }
 
 // The same for a warp that runs converged: lane 0 polls, every lane gets the
 // outcome (and elect.sync later picks lane 0, the lane that observed it).
-__device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, const Params& p, Bars* bs) {
+__device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, const Params& p, Bars* bs, int site) {
   bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, p, bs);
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, p, bs, site);
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
 // The same for the row warps' progress counters: every lane < kRowWarps polls
 // one counter until all have reached `target` (bounded like wait_bar).
-__device__ __forceinline__ bool wait_counters(const uint32_t* ctr, uint32_t target, const Params& p, Bars* bs) {
+__device__ __forceinline__ bool wait_counters(const uint32_t* ctr, uint32_t target, const Params& p, Bars* bs,
+                                              int site) {
   const int lane = threadIdx.x & 31;
   for (long long i = 0;; ++i) {
     const bool mine = lane >= kRowWarps || static_cast<int32_t>(ld_acquire_u32(ctr + lane) - target) >= 0;
     if (__all_sync(0xffffffffu, mine)) return true;
-    if (i >= p.wait_limit || *reinterpret_cast<volatile int*>(&bs->abort)) {
-      if (lane == 0) {
-        report(p.status, MLA_ERR_DEVICE_TIMEOUT);
-        atomicExch(&bs->abort, 1);
-      }
-      return false;
-    }
+    bool out = false;
+    if (lane == 0) out = timed_out(i, p, bs, site);
+    if (__shfl_sync(0xffffffffu, out ? 1 : 0, 0)) return false;
   }
 }
 
 // All lanes of a warp poll one counter until it reaches `target` (bounded).
-__device__ __forceinline__ bool wait_counter(const uint32_t* ctr, uint32_t target, const Params& p, Bars* bs) {
+__device__ __forceinline__ bool wait_counter(const uint32_t* ctr, uint32_t target, const Params& p, Bars* bs,
+                                             int site) {
   for (long long i = 0;; ++i) {
     if (static_cast<int32_t>(ld_acquire_u32(ctr) - target) >= 0) return true;
-    if (i >= p.wait_limit || *reinterpret_cast<volatile int*>(&bs->abort)) {
-      report(p.status, MLA_ERR_DEVICE_TIMEOUT);
-      atomicExch(&bs->abort, 1);
-      return false;
-    }
+    if (timed_out(i, p, bs, site)) return false;
   }
 }
 
@@ -318,9 +326,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       while (ok && iter.next(p, g, u)) {
         for (int t = u.ta; t < u.tb && ok; ++t, ++it) {
           const int s = it % kStages;
-          if (it >= kStages) ok = wait_bar(&bs->empty[s], ((it / kStages) - 1) & 1, p, bs);
+          if (it >= kStages) ok = wait_bar(&bs->empty[s], ((it / kStages) - 1) & 1, p, bs, 1);
           const int rs = it % kRopeSlots;
-          if (ok && it >= kRopeSlots) ok = wait_bar(&bs->rope_empty[rs], ((it / kRopeSlots) - 1) & 1, p, bs);
+          if (ok && it >= kRopeSlots) ok = wait_bar(&bs->rope_empty[rs], ((it / kRopeSlots) - 1) & 1, p, bs, 2);
           if (!ok) break;
           const int y = tile_row(u.b, t);
           uint8_t* st = smem + kOffStages + s * kStageBytes;
@@ -350,14 +358,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t n_units = 0;
       bool ok = true;
       while (ok && iter.next(p, g, u)) {
-        ok = wait_counters(bs->n_q, n_units + 1, p, bs);
+        ok = wait_counters(bs->n_q, n_units + 1, p, bs, 3);
         ++n_units;
         if (!ok) break;
         tc_fence_after();
         for (int t = u.ta; t < u.tb && ok; ++t, ++k) {
           // S(k) into the single S buffer once the row warps have read S(k-1) out of it
-          if (!(ok = wait_bar_warp(&bs->full[k % kStages], (k / kStages) & 1, p, bs))) break;
-          if (k >= 1 && !(ok = wait_counters(bs->n_s_read, k, p, bs))) break;
+          if (!(ok = wait_bar_warp(&bs->full[k % kStages], (k / kStages) & 1, p, bs, 4))) break;
+          if (k >= 1 && !(ok = wait_counters(bs->n_s_read, k, p, bs, 5))) break;
           tc_fence_after();
           const uint32_t st = smem_u32(smem + kOffStages + (k % kStages) * kStageBytes);
           const uint32_t rope = smem_u32(smem + kOffRope + (k % kRopeSlots) * kRopeBoxBytes);
@@ -386,7 +394,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       while (ok && iter.next(p, g, u)) {
         for (int t = u.ta; t < u.tb && ok; ++t, ++k) {
           // P(k) is in TMEM (and S(k) done, so the stage has landed)
-          if (!(ok = wait_counters(bs->n_p_done, k + 1, p, bs))) break;
+          if (!(ok = wait_counters(bs->n_p_done, k + 1, p, bs, 6))) break;
           tc_fence_after();
           const uint32_t st = smem_u32(smem + kOffStages + (k % kStages) * kStageBytes);
           mma_value_tile_elect<kTile / 16>(tmem + kTmemO, tmem + kTmemP, smem_desc(st, kBoxBytes, 1024, kSwizzle128B),
@@ -436,7 +444,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // Reads this thread's 32 scores of S out of TMEM, scaled to log2 units
     // (kept in `own`, fp32), and hands their fp16 rounding to the exchange warp.
     auto send = [&](float2* own) -> bool {
-      if (!wait_bar(&bs->s_full, n_s & 1, p, bs)) return false;
+      if (!wait_bar(&bs->s_full, n_s & 1, p, bs, 12)) return false;
       ++n_s;
       tc_fence_after();
       uint32_t v[32];
@@ -452,7 +460,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         h[k] = pack_half2(own[k].x, own[k].y);
       }
       // the exchange warp's copy of the previous block has read the outbox
-      if (n_send >= 1 && !wait_counter(&bs->n_out_free[rw], n_send, p, bs)) return false;
+      if (n_send >= 1 && !wait_counter(&bs->n_out_free[rw], n_send, p, bs, 10)) return false;
       uint8_t* row = outbox + lane * 64;
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch)
@@ -506,7 +514,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ---- 1. s = own + peer partial scores of this tile (log2 units)
         const uint32_t rslot = n_recv & 1;
         {
-          if (!(ok = wait_bar(&bs->xin_full[rslot][rw], (n_recv >> 1) & 1, p, bs, true))) break;
+          if (!(ok = wait_bar(&bs->xin_full[rslot][rw], (n_recv >> 1) & 1, p, bs, 13, true))) break;
           ++n_recv;
           if (lane == 0) mbar_arrive_expect_tx(&bs->xin_full[rslot][rw], kXBlockBytes);  // arm the next phase
           const uint8_t* row = inbox0 + rslot * kXSlotBytes + lane * 64;
@@ -563,7 +571,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ma = mua;
         mb = mub;
         // ---- 3. the previous O MMA is done (P is free); rescale O if a max moved; write P
-        if (n_p >= 1 && !(ok = wait_bar(&bs->p_free, (n_p - 1) & 1, p, bs))) break;
+        if (n_p >= 1 && !(ok = wait_bar(&bs->p_free, (n_p - 1) & 1, p, bs, 14))) break;
         tc_fence_after();
         if (__any_sync(0xffffffffu, fa != 1.f || fb != 1.f)) {
 #pragma unroll 1
@@ -603,13 +611,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       lb += __shfl_xor_sync(0xffffffffu, lb, 1);
       la += __shfl_xor_sync(0xffffffffu, la, 2);
       lb += __shfl_xor_sync(0xffffffffu, lb, 2);
-      if (!(ok = wait_bar(&bs->p_free, (n_p - 1) & 1, p, bs))) break;
+      if (!(ok = wait_bar(&bs->p_free, (n_p - 1) & 1, p, bs, 17))) break;
       tc_fence_after();
       const float inv_la = 1.f / la, inv_lb = 1.f / lb;
       // O leaves TMEM in 32-column chunks staged through this warp's (idle)
       // outbox block (16 rows x 128 B fp32, 8-byte slots XOR-swizzled by row)
       // so that every global store covers whole row segments.
-      if (!(ok = wait_counter(&bs->n_out_free[rw], n_send, p, bs))) break;  // no copy still reads the outbox
+      if (!(ok = wait_counter(&bs->n_out_free[rw], n_send, p, bs, 16))) break;  // no copy still reads the outbox
       uint8_t* const stg = outbox;
       const int ra = lane >> 2;  // staging rows ra (head ha) and ra + 8 (head ha + 8)
       const size_t row0 = static_cast<size_t>(u.slot < 0 ? u.n : u.slot) * kHeads + q * 32 + hh * 16;
@@ -663,11 +671,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     while (ok && iter.next(p, g, u)) {
       for (int t = u.ta; t < u.tb && ok; ++t, ++i) {
-        if (!(ok = wait_counters(bs->n_out_ready, i + 1, p, bs))) break;
+        if (!(ok = wait_counters(bs->n_out_ready, i + 1, p, bs, 7))) break;
         const uint32_t slot = i & 1;
         bool good = true;
         if (lane < kRowWarps) {
-          if (i >= 2) good = wait_bar(&bs->inbox_free[slot][rw], ((i >> 1) - 1) & 1, p, bs, true);
+          if (i >= 2) good = wait_bar(&bs->inbox_free[slot][rw], ((i >> 1) - 1) & 1, p, bs, 8, true);
           if (good) {
             bulk_copy_to_peer(peer_inbox_rw + slot * kXSlotBytes, outbox_rw, kXBlockBytes, peer_xin_rw + slot * kBarSlot);
             bulk_commit();
@@ -683,7 +691,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane < kRowWarps) {
       bulk_wait_all();
       for (uint32_t k = (i > 2 ? i - 2 : 0); ok && k < i; ++k)
-        ok = wait_bar(&bs->inbox_free[k & 1][rw], (k >> 1) & 1, p, bs, true);
+        ok = wait_bar(&bs->inbox_free[k & 1][rw], (k >> 1) & 1, p, bs, 9, true);
     }
   }
 
@@ -820,20 +828,35 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ seq_
 // Merge the pieces of every token whose keys were split across workers:
 // lse = ln sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s (the standard
 // identity for a softmax split over disjoint key ranges; not on the pages).
-// One warp per (token, head); the pieces of a token are the workers g0..g1
+// One CTA per (token, head); the pieces of a token are the workers g0..g1
 // whose ranges meet its tiles.  Worker g wrote slot 2g when its range starts
-// inside the token, else 2g+1 (its range started in an earlier token).
-__global__ void __launch_bounds__(256) combine_kernel(const int* __restrict__ prefix, const int* __restrict__ plan_flags,
-                                                      int n_tok, int workers, const float* __restrict__ part_o,
-                                                      const float* __restrict__ part_lse,
-                                                      __nv_bfloat16* __restrict__ o_lat, float* __restrict__ lse) {
+// inside the token, else 2g+1 (its range started in an earlier token).  The
+// pieces are spread over the CTA's eight warps (each lane holds 16 of the 512
+// columns), so their loads are in flight together; the warps' sums meet in
+// shared memory.
+__device__ __forceinline__ int piece_slot(int k, int g0, int t0, int workers, int total) {
+  const int g = g0 + k;
+  int lo, hi;
+  worker_range(g, workers, total, lo, hi);
+  if (lo >= hi) return -1;  // an empty range wrote nothing
+  return (k == 0 && lo < t0) ? 2 * g + 1 : 2 * g;
+}
+
+constexpr int kCombineWarps = 8;
+
+__global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(
+    const int* __restrict__ prefix, const int* __restrict__ plan_flags, int n_tok, int workers,
+    const float* __restrict__ part_o, const float* __restrict__ part_lse, __nv_bfloat16* __restrict__ o_lat,
+    float* __restrict__ lse) {
+  __shared__ float s_red[kCombineWarps];
+  __shared__ float4 s_acc[kCombineWarps][kDc / 4];
   pdl_wait();
   // The next decode call's plan may overwrite the plan data, so the next
   // kernel may launch only once every CTA has read all of it: CTAs that stop
   // here exit (an exit counts as the trigger); the others trigger after the
   // checks below have consumed every value they read.
   if (__ldg(plan_flags) == 0) return;  // whole tokens per worker: nothing was split
-  const int n = blockIdx.x;
+  const int n = blockIdx.x, h = blockIdx.y;
   const int total = __ldg(prefix + n_tok);
   const int t0 = __ldg(prefix + n), t1 = __ldg(prefix + n + 1);
   if (t1 <= t0) return;
@@ -842,66 +865,63 @@ __global__ void __launch_bounds__(256) combine_kernel(const int* __restrict__ pr
   __syncthreads();
   if (threadIdx.x == 0) pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y * 8 + warp;
-  // lane k < npieces holds piece k's slot and lse
   const int npieces = g1 - g0 + 1;
-  float mx = -INFINITY, my_lse = -INFINITY;
-  int my_slot = -1;
-  for (int k = lane; k < npieces; k += 32) {
-    const int g = g0 + k;
-    int lo, hi;
-    worker_range(g, workers, total, lo, hi);
-    int slot = -1;
-    if (lo < hi) slot = (k == 0 && lo < t0) ? 2 * g + 1 : 2 * g;
-    if (slot >= 0) {
-      const float v = __ldg(part_lse + static_cast<size_t>(slot) * kHeads + h);
-      mx = fmaxf(mx, v);
-      if (k < 32) { my_slot = slot; my_lse = v; }
-    }
+  // L = ln sum_s exp(lse_s), block-wide: max, then the sum of exponentials
+  float mx = -INFINITY;
+  for (int k = threadIdx.x; k < npieces; k += blockDim.x) {
+    const int slot = piece_slot(k, g0, t0, workers, total);
+    if (slot >= 0) mx = fmaxf(mx, __ldg(part_lse + static_cast<size_t>(slot) * kHeads + h));
   }
   mx = warp_max(mx);
-  float sum = (my_slot >= 0) ? expf(my_lse - mx) : 0.f;
-  for (int k = lane + 32; k < npieces; k += 32) {  // more than 32 pieces: rare, recompute
-    const int g = g0 + k;
-    int lo, hi;
-    worker_range(g, workers, total, lo, hi);
-    if (lo < hi) sum += expf(__ldg(part_lse + static_cast<size_t>(2 * g) * kHeads + h) - mx);
+  if (lane == 0) s_red[warp] = mx;
+  __syncthreads();
+  mx = s_red[0];
+#pragma unroll
+  for (int w = 1; w < kCombineWarps; ++w) mx = fmaxf(mx, s_red[w]);
+  __syncthreads();
+  float sum = 0.f;
+  for (int k = threadIdx.x; k < npieces; k += blockDim.x) {
+    const int slot = piece_slot(k, g0, t0, workers, total);
+    if (slot >= 0) sum += expf(__ldg(part_lse + static_cast<size_t>(slot) * kHeads + h) - mx);
   }
   sum = warp_sum(sum);
-  const float L = mx + logf(sum);
-  float acc[16];
+  if (lane == 0) s_red[warp] = sum;
+  __syncthreads();
+  sum = 0.f;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-  for (int k = 0; k < npieces; ++k) {
-    int slot;
-    float ls;
-    if (k < 32) {
-      slot = __shfl_sync(0xffffffffu, my_slot, k);
-      ls = __shfl_sync(0xffffffffu, my_lse, k);
-    } else {
-      const int g = g0 + k;
-      int lo, hi;
-      worker_range(g, workers, total, lo, hi);
-      slot = lo < hi ? 2 * g : -1;
-      ls = slot >= 0 ? __ldg(part_lse + static_cast<size_t>(slot) * kHeads + h) : -INFINITY;
-    }
+  for (int w = 0; w < kCombineWarps; ++w) sum += s_red[w];
+  const float L = mx + logf(sum);
+  // o = sum_s exp(lse_s - L) o_s: warp w takes pieces w, w + 8, ...
+  float4 acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+  for (int k = warp; k < npieces; k += kCombineWarps) {
+    const int slot = piece_slot(k, g0, t0, workers, total);
     if (slot < 0) continue;
-    const float w = expf(ls - L);
+    const float wk = expf(__ldg(part_lse + static_cast<size_t>(slot) * kHeads + h) - L);
     const float4* src = reinterpret_cast<const float4*>(part_o + (static_cast<size_t>(slot) * kHeads + h) * kDc);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float4 v = __ldg(src + lane + 32 * j);
-      acc[4 * j] += w * v.x; acc[4 * j + 1] += w * v.y; acc[4 * j + 2] += w * v.z; acc[4 * j + 3] += w * v.w;
+      acc[j].x += wk * v.x; acc[j].y += wk * v.y; acc[j].z += wk * v.z; acc[j].w += wk * v.w;
     }
   }
-  __nv_bfloat16* dst = o_lat + (static_cast<size_t>(n) * kHeads + h) * kDc;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int col = 4 * (lane + 32 * j);
-    reinterpret_cast<uint2*>(dst + col)[0] = make_uint2(pack_bf16x2(acc[4 * j], acc[4 * j + 1]),
-                                                        pack_bf16x2(acc[4 * j + 2], acc[4 * j + 3]));
+  for (int j = 0; j < 4; ++j) s_acc[warp][lane + 32 * j] = acc[j];
+  __syncthreads();
+  // thread i finishes the 4 columns of float4 slot i (i < 128) of the 512
+  if (threadIdx.x < kDc / 4) {
+    float4 o = s_acc[0][threadIdx.x];
+#pragma unroll
+    for (int w = 1; w < kCombineWarps; ++w) {
+      const float4 v = s_acc[w][threadIdx.x];
+      o.x += v.x; o.y += v.y; o.z += v.z; o.w += v.w;
+    }
+    __nv_bfloat16* dst = o_lat + (static_cast<size_t>(n) * kHeads + h) * kDc + 4 * threadIdx.x;
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
   }
-  if (lane == 0) lse[static_cast<size_t>(n) * kHeads + h] = L;
+  if (threadIdx.x == 0) lse[static_cast<size_t>(n) * kHeads + h] = L;
 }
 
 bool encode_pool_maps(const mla_handle* h, Maps* maps, const void* pool, long long rows) {
@@ -921,7 +941,7 @@ cudaError_t launch_decode_kernels(const mla_handle* h, const Maps& maps, const P
   if (e != cudaSuccess) return e;
   e = launch_pdl(decode_tc_kernel, dim3(2 * W), dim3(kThreads), kSmemBytes, s, 1, maps, prm);
   if (e != cudaSuccess) return e;
-  return launch_pdl(combine_kernel, dim3(n_tok, kHeads / 8), dim3(256), 0, s, 1, static_cast<const int*>(prm.prefix),
+  return launch_pdl(combine_kernel, dim3(n_tok, kHeads), dim3(32 * kCombineWarps), 0, s, 1, static_cast<const int*>(prm.prefix),
                     prm.plan_flags, n_tok, W, static_cast<const float*>(prm.part_o), static_cast<const float*>(prm.part_lse), prm.o_lat,
                     lse);
 }
@@ -1010,7 +1030,7 @@ __global__ void wait_timeout_selftest_kernel(int* status, long long wait_limit) 
   if (threadIdx.x == 0) {
     bool done = false;
     for (long long i = 0; i < wait_limit && !done; ++i) done = mbar_try_wait(&bar, 0);
-    if (!done) report(status, MLA_ERR_DEVICE_TIMEOUT);
+    if (!done) report_site(status, 1, -1);
     mbar_arrive(&bar);  // complete the phase so the barrier is idle at exit
   }
 }

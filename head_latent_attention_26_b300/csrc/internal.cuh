@@ -45,7 +45,9 @@ struct mla_handle {
   int num_sms;
   float* rope_cos;  // [max_pos, d_hr/2], cos(pos * base^(-2k/d_hr)) rounded from double
   float* rope_sin;
-  int* status;      // first device-side error code, 0 = none
+  int* status;      // [4]: first device-side error code (0 = none), then where the first
+                    // bounded wait gave up: site word, CTA, tile (see report_site)
+  int last_site[3];  // the site words read back by the last mla_check_device_status
   long long wait_limit;
   bool tensor_path;  // tcgen05 decode serves these dims
   bool proj_tc;      // tcgen05 projection kernels serve these dims
@@ -65,6 +67,17 @@ constexpr long long kDefaultWaitLimit = 1ll << 24;  // mbarrier polls (about 0.1
 
 // Records `code` in the status word unless an earlier error is already there.
 __device__ __forceinline__ void report(int* status, int code) { atomicCAS(status, 0, code); }
+// A bounded wait ran out: records MLA_ERR_DEVICE_TIMEOUT and, for the first
+// such wait of the call, which one it was (a site number of the kernel, the
+// warp), the CTA and the tile it waited for.
+__device__ __forceinline__ void report_site(int* status, int site, int k) {
+  report(status, MLA_ERR_DEVICE_TIMEOUT);
+  const int word = 0x40000000 | (site << 8) | static_cast<int>(threadIdx.x >> 5);
+  if (atomicCAS(status + 1, 0, word) == 0) {
+    status[2] = static_cast<int>(blockIdx.x);
+    status[3] = k;
+  }
+}
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }

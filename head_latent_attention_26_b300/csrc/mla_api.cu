@@ -131,10 +131,10 @@ mla_status mla_create(const mla_dims* dims, int max_pos, mla_handle** out) {
     }
   bool ok = cudaMalloc(&h->rope_cos, n * sizeof(float)) == cudaSuccess &&
             cudaMalloc(&h->rope_sin, n * sizeof(float)) == cudaSuccess &&
-            cudaMalloc(&h->status, sizeof(int)) == cudaSuccess &&
+            cudaMalloc(&h->status, 4 * sizeof(int)) == cudaSuccess &&
             cudaMemcpy(h->rope_cos, c.data(), n * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemcpy(h->rope_sin, s.data(), n * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess &&
-            cudaMemset(h->status, 0, sizeof(int)) == cudaSuccess;
+            cudaMemset(h->status, 0, 4 * sizeof(int)) == cudaSuccess;
   // The fixed scratch of mla_decode_noalloc: its device address on this
   // device, looked up now with the device current.  The lookup also loads the
   // library's device code here, so the array is reserved at creation rather
@@ -343,10 +343,21 @@ mla_status mla_out(mla_handle* h, const void* o_lat, const void* w_uv, const voi
 mla_status mla_check_device_status(mla_handle* h, cudaStream_t stream) {
   if (!h) return MLA_ERR_INVALID_ARG;
   MLA_TRY_CUDA(cudaStreamSynchronize(stream));
-  int v = 0;
-  MLA_TRY_CUDA(cudaMemcpy(&v, h->status, sizeof(int), cudaMemcpyDeviceToHost));
-  MLA_TRY_CUDA(cudaMemset(h->status, 0, sizeof(int)));
-  return static_cast<mla_status>(v);
+  int v[4] = {0, 0, 0, 0};
+  MLA_TRY_CUDA(cudaMemcpy(v, h->status, sizeof(v), cudaMemcpyDeviceToHost));
+  MLA_TRY_CUDA(cudaMemset(h->status, 0, sizeof(v)));
+  h->last_site[0] = v[1];
+  h->last_site[1] = v[2];
+  h->last_site[2] = v[3];
+  return static_cast<mla_status>(v[0]);
+}
+
+mla_status mla_device_error_site(const mla_handle* h, int* site, int* cta, int* tile) {
+  if (!h || !site || !cta || !tile) return MLA_ERR_INVALID_ARG;
+  *site = h->last_site[0];
+  *cta = h->last_site[1];
+  *tile = h->last_site[2];
+  return MLA_OK;
 }
 
 mla_status mla_selftest_wait_timeout(mla_handle* h, cudaStream_t stream) {

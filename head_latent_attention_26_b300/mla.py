@@ -67,6 +67,7 @@ _SIGS = {
     "mla_out": (I, [P, P, P, P, I, P, P, SZ, P]),
     "mla_check_device_status": (I, [P, P]),
     "mla_selftest_wait_timeout": (I, [P, P]),
+    "mla_device_error_site": (I, [P, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)]),
 }
 
 
@@ -159,6 +160,14 @@ class MLA:
 
     def device_status(self) -> int:
         return self.lib.mla_check_device_status(self.h, P(_stream()))
+
+    def error_site(self):
+        """(site word, CTA, tile) of the first bounded wait that ran out, as
+        read back by the last check (site word 0 = none)."""
+        a, b, c = I(), I(), I()
+        _check(self.lib.mla_device_error_site(self.h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
+               "mla_device_error_site")
+        return a.value, b.value, c.value
 
     def selftest_wait_timeout(self) -> int:
         _check(self.lib.mla_selftest_wait_timeout(self.h, P(_stream())), "selftest launch")

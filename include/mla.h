@@ -230,6 +230,14 @@ mla_status mla_out(mla_handle* h, const void* o_lat, const void* w_uv, const voi
  * device status word since the last check (MLA_OK if none) and clears it. */
 mla_status mla_check_device_status(mla_handle* h, cudaStream_t stream);
 
+/* Where the first bounded wait that ran out (MLA_ERR_DEVICE_TIMEOUT) gave up,
+ * as read back by the last mla_check_device_status: *site = 0 when none did,
+ * else 0x40000000 | (wait site within its kernel << 8) | warp; *cta = the
+ * CTA's linear index; *tile = the tile it waited for, or -1 where the kernel
+ * does not record it.
+ * Diagnostic only; the sites are numbered in the kernels' sources. */
+mla_status mla_device_error_site(const mla_handle* h, int* site, int* cta, int* tile);
+
 /* Runs one kernel that waits on a barrier no one arrives at, with the
  * handle's wait limit; it must come back with MLA_ERR_DEVICE_TIMEOUT recorded
  * in the status word.  Exercises the bounded-wait path without a fault. */
