@@ -78,7 +78,6 @@ constexpr int kTile = 64;               // keys per tile = rows per cache block
 constexpr int kBlockRows = 64;
 constexpr int kWidth = 576;             // d_c + d_hr
 constexpr int kDc = 512;
-constexpr int kStages = 5;             // latent stages (32 KB each)
 constexpr int kRopeSlots = 3;          // RoPE boxes live only until their score MMA
 constexpr uint32_t kBoxBytes = kTile * 128;                 // 64 keys x 64 cols bf16 (128B swizzle)
 constexpr uint32_t kRopeBoxBytes = kTile * 64;              // 64 keys x 32 cols bf16 (64B swizzle)
@@ -86,12 +85,34 @@ constexpr uint32_t kStageBytes = 4 * kBoxBytes;             // 32768: the latent
 constexpr int kRowWarps = 8;                                // softmax warps: 16 heads each
 constexpr uint32_t kXBlockBytes = 16 * kTile * 2;           // one warp's 16 heads x 64 keys fp16
 constexpr uint32_t kXSlotBytes = kRowWarps * kXBlockBytes;  // all row warps
-constexpr uint32_t kOffStages = 0;
-constexpr uint32_t kOffRope = kOffStages + kStages * kStageBytes;
-constexpr uint32_t kOffInbox = kOffRope + kRopeSlots * kRopeBoxBytes;
-constexpr uint32_t kOffOutbox = kOffInbox + 2 * kXSlotBytes;  // one slot: a copy reads it long before reuse
-constexpr uint32_t kOffBars = kOffOutbox + kXSlotBytes;
-constexpr uint32_t kSmemBytes = kOffBars + 1024 + 1024;     // + alignment slack
+// Quantised cache rows (672 bytes: 512 int8 codes | 16 fp16 scales | 64 bf16
+// k^R): a CTA's raw slot holds its 256 codes and 8 scales of every row of a tile.
+constexpr int kQ8RowBytes = 672;
+constexpr uint32_t kCodeBytes = kTile * 256, kScaleBytes = kTile * 16;
+constexpr uint32_t kRawBytes = kCodeBytes + kScaleBytes + kRopeBoxBytes;  // codes | scales | RoPE box
+
+// Shared memory of the two cache formats.  bf16 rows: five stages of the
+// tile's latent columns and three RoPE slots.  Quantised rows: three raw
+// slots (codes, scales and RoPE box as loaded) and three fp16 stages they are
+// turned into, each with its RoPE box after the latent columns (so a stage
+// and its RoPE box are freed together).
+constexpr int kMaxRawSlots = 3;
+template <bool Q8>
+struct Layout {
+  static constexpr int kStages = Q8 ? 3 : 5;
+  static constexpr int kRawSlots = Q8 ? kMaxRawSlots : 0;
+  static constexpr uint32_t kStageStride = kStageBytes + (Q8 ? kRopeBoxBytes : 0);
+  static constexpr uint32_t kOffStages = 0;
+  static constexpr uint32_t kOffRaw = kOffStages + kStages * kStageStride;
+  static constexpr uint32_t kOffRope = kOffRaw + kRawSlots * kRawBytes;  // bf16 rows: the RoPE slots
+  static constexpr uint32_t kOffInbox = kOffRope + (Q8 ? 0 : kRopeSlots * kRopeBoxBytes);
+  static constexpr uint32_t kOffOutbox = kOffInbox + 2 * kXSlotBytes;  // one slot: a copy reads it long before reuse
+  static constexpr uint32_t kOffBars = kOffOutbox + kXSlotBytes;
+  static constexpr uint32_t kSmemBytes = kOffBars + 1024 + 1024;     // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert(kOffRaw % 1024 == 0 && kRawBytes % 1024 == 0 && kOffRope % 1024 == 0, "TMA destinations");
+};
+constexpr int kMaxStages = 5;
 // TMEM columns (512 allocated): O half | Q~ latent half | Q~ RoPE half | P | S
 // (bf16 operands hold two elements per 32-bit column)
 constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemQR = 384, kTmemP = 416, kTmemS = 448;
@@ -103,8 +124,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct Maps {
-  CUtensorMap latent;  // pool as [rows, 576] bf16, box 64 cols x 64 rows, 128B swizzle
-  CUtensorMap rope;    // same tensor, box 32 cols x 64 rows, 64B swizzle
+  CUtensorMap latent;  // bf16 pool as [rows, 576], box 64 cols x 64 rows, 128B swizzle
+  CUtensorMap rope;    // the RoPE columns: bf16 box 32 cols x 64 rows, or the same 64 bytes of a quantised row; 64B swizzle
+  CUtensorMap codes;   // quantised pool as [rows, 672] bytes: box 256 x 64 rows (a CTA's codes)
+  CUtensorMap scales;  // the same tensor: box 16 x 64 rows (a CTA's 8 scales)
 };
 
 struct Params {
@@ -127,7 +150,8 @@ struct Params {
 };
 
 struct Bars {
-  uint64_t full[kStages], empty[kStages], rope_empty[kRopeSlots];
+  uint64_t full[kMaxStages], empty[kMaxStages], rope_empty[kRopeSlots];
+  uint64_t raw_full[kMaxRawSlots], raw_empty[kMaxRawSlots];  // quantised cache: raw slot loaded / turned into a stage
   uint64_t s_full, p_free;
   // progress counters of the row warps, polled by the MMA issuers: query
   // tokens loaded into TMEM, S tiles read out of TMEM, P tiles written
@@ -259,8 +283,140 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Physical pool row of tile t of sequence b (a bad table entry is reported
+// and replaced by block 0).
+__device__ __forceinline__ int tile_row(const Params& p, int b, int t) {
+  int blk = t < p.max_blocks ? __ldg(p.block_table + static_cast<size_t>(b) * p.max_blocks + t) : -1;
+  if (blk < 0 || blk >= p.n_pool_blocks) {
+    report(p.status, MLA_ERR_DEVICE_BOUNDS);
+    blk = 0;
+  }
+  return blk * kBlockRows;
+}
+
+// Two int8 codes of w (bytes j, j + 1) times the fp16 scale d2, as fp16x2:
+// each biased code u = code + 128 goes into the mantissa of the fp16 number
+// 1024 + u (one byte permute), 1152 is subtracted (exact: an integer below
+// 2048) and the product with the scale is rounded once.
+__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t w_biased, uint32_t sel, __half2 d2) {
+  const uint32_t bits = __byte_perm(w_biased, 0x64646464u, sel);
+  const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&bits), __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+  const __half2 r = __hmul2(v, d2);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+// Two bf16 values (one 32-bit word) as fp16x2 (exact for fp16-range values).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  const __half2 r = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// Quantised cache, warps 0 and 3: turn every tile's int8 codes into the fp16
+// stage the MMAs read (the quantised path multiplies in fp16: an 11-bit
+// mantissa keeps code x scale within one rounding of 2^-11).  Warp 0 converts
+// rows 0..31 and warp 3 rows 32..63 of the tile (lane = a group of 8
+// columns; value = code x its run's fp16 scale, rounded once, written in the
+// 128B-swizzled layout a TMA load of 16-bit rows would give) and the same
+// rows of the RoPE box, bf16 to fp16 in place; lane 0 of warp 0 also issues
+// the TMA loads of the codes, scales and RoPE box, kRawSlots tiles ahead.
+__device__ __noinline__ void dequantise_role(const Maps& maps, const Params& p, Bars* bs, uint8_t* smem, int g,
+                                             uint32_t c, int warp, int lane) {
+  using L = Layout<true>;
+  const int half = warp == 0 ? 0 : 1;
+  const bool loader = warp == 0 && lane == 0;
+  const int4 wp = __ldg(reinterpret_cast<const int4*>(p.worker_plan) + g);
+  const uint32_t total = wp.y > wp.x ? static_cast<uint32_t>(wp.y - wp.x) : 0u;
+  const uint64_t pol = l2_policy_evict_first();  // every cache row is read once
+  UnitIter li = make_iter(p, g);
+  Unit lu;
+  int lt = 0, lt_end = 0;
+  uint32_t lit = 0;  // tiles whose loads were issued
+  // issues the loads of the next tile of this worker (lane 0 of warp 0)
+  auto load_next = [&]() -> bool {
+    while (lt >= lt_end) {
+      if (!li.next(p, g, lu)) return true;
+      lt = lu.ta;
+      lt_end = lu.tb;
+    }
+    constexpr uint32_t R = L::kRawSlots;
+    const uint32_t r = lit % R;
+    if (lit >= R && !wait_bar(&bs->raw_empty[r], ((lit / R) - 1) & 1, p, bs, 19)) return false;
+    const int y = tile_row(p, lu.b, lt);
+    uint8_t* raw = smem + L::kOffRaw + r * kRawBytes;
+    mbar_arrive_expect_tx(&bs->raw_full[r], kRawBytes);
+    tma_load_2d_hint(raw, &maps.codes, &bs->raw_full[r], 256 * c, y, pol);
+    tma_load_2d_hint(raw + kCodeBytes, &maps.scales, &bs->raw_full[r], kDc + 16 * c, y, pol);
+    tma_load_2d_hint(raw + kCodeBytes + kScaleBytes, &maps.rope, &bs->raw_full[r], kDc + 32 + 64 * c, y, pol);
+    ++lt;
+    ++lit;
+    return true;
+  };
+  bool ok = true;
+  if (loader) {
+    tma_prefetch_desc(&maps.codes);
+    tma_prefetch_desc(&maps.scales);
+    tma_prefetch_desc(&maps.rope);
+    for (int i = 0; i < L::kRawSlots && ok; ++i) ok = load_next();
+  }
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  const int box = lane >> 3, chunk = lane & 7;  // this lane's 8 columns: box `box`, 16-byte chunk `chunk`
+  for (uint32_t k = 0; k < total && ok; ++k) {
+    if (!(ok = wait_bar_warp(&bs->raw_full[k % L::kRawSlots], (k / L::kRawSlots) & 1, p, bs, 20))) break;
+    const int s = k % L::kStages;
+    if (k >= L::kStages && !(ok = wait_bar_warp(&bs->empty[s], ((k / L::kStages) - 1) & 1, p, bs, 1))) break;
+    const uint8_t* raw = smem + L::kOffRaw + (k % L::kRawSlots) * kRawBytes;
+    uint8_t* st = smem + L::kOffStages + s * L::kStageStride + box * kBoxBytes;
+#pragma unroll 4
+    for (int i = 0; i < 32; ++i) {
+      const int r = 32 * half + i;
+      const uint2 cw = *reinterpret_cast<const uint2*>(raw + r * 256 + lane * 8);
+      const __half d = *reinterpret_cast<const __half*>(raw + kCodeBytes + r * 16 + (lane >> 2) * 2);
+      const __half2 d2 = __halves2half2(d, d);
+      const uint32_t x0 = cw.x ^ 0x80808080u, x1 = cw.y ^ 0x80808080u;  // code + 128 in every byte
+      const uint4 o = make_uint4(codes_to_f16x2(x0, 0x4140u, d2), codes_to_f16x2(x0, 0x4342u, d2),
+                                 codes_to_f16x2(x1, 0x4140u, d2), codes_to_f16x2(x1, 0x4342u, d2));
+      *reinterpret_cast<uint4*>(st + r * 128 + ((chunk ^ (r & 7)) * 16)) = o;
+    }
+    {
+      // the RoPE box, rows [32 half, 32 half + 32) (2 KB, 512 contiguous
+      // bytes a pass of the warp), into the stage's RoPE box at the same
+      // (swizzled) positions
+      const uint4* rs = reinterpret_cast<const uint4*>(raw + kCodeBytes + kScaleBytes + half * 2048);
+      uint4* rd = reinterpret_cast<uint4*>(smem + L::kOffStages + s * L::kStageStride + kStageBytes + half * 2048);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 w = rs[32 * j + lane];
+        rd[32 * j + lane] =
+            make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+      }
+    }
+    fence_proxy_async_smem();  // the MMAs read the stage through the async proxy
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&bs->full[s]);
+      mbar_arrive(&bs->raw_empty[k % L::kRawSlots]);
+    }
+    if (warp == 0) {
+      bool okl = true;
+      if (loader && lit < total) okl = load_next();
+      ok = __shfl_sync(0xffffffffu, okl ? 1 : 0, 0) != 0;
+    }
+  }
+  // every issued load must land before the CTA may exit
+  if (!ok && loader) {
+    constexpr uint32_t R = L::kRawSlots;
+    for (uint32_t k = lit > R ? lit - R : 0; k < lit; ++k)
+      for (long long i = 0; i < p.wait_limit && !mbar_try_wait(&bs->raw_full[k % R], (k / R) & 1); ++i) {
+      }
+  }
+}
+
+template <bool Q8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ Maps maps, const Params p) {
+  using L = Layout<Q8>;
+  constexpr int kStages = L::kStages;
+  constexpr uint32_t kOffStages = L::kOffStages, kOffRope = L::kOffRope, kOffInbox = L::kOffInbox;
+  constexpr uint32_t kOffOutbox = L::kOffOutbox, kOffBars = L::kOffBars;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bs = reinterpret_cast<Bars*>(smem + kOffBars);
@@ -271,8 +427,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bs->full[s], 1);
+      mbar_init(&bs->full[s], Q8 ? 2 : 1);  // quantised cache: the two warps that turn codes into the stage
       mbar_init(&bs->empty[s], 1);
+    }
+    for (int r = 0; r < kMaxRawSlots; ++r) {
+      mbar_init(&bs->raw_full[r], 1);
+      mbar_init(&bs->raw_empty[r], 2);
     }
     for (int s = 0; s < kRopeSlots; ++s) mbar_init(&bs->rope_empty[s], 1);
     mbar_init(&bs->s_full, 1);
@@ -303,22 +463,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bs->tmem_base;
   pdl_wait();  // the plan, the latent queries and the cache rows are written by earlier kernels
 
-  if (warp == 0) {
+  if (Q8 && (warp == 0 || warp == kXchgWarp)) {
+    // ------------------------------------------------------------ quantised cache: loads and dequantisation
+    if constexpr (Q8) dequantise_role(maps, p, bs, smem, g, c, warp, lane);
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&maps.latent);
       tma_prefetch_desc(&maps.rope);
       const uint64_t pol = l2_policy_evict_first();  // every cache row is read once
-      // Physical pool row of tile t of sequence b (a bad table entry is
-      // reported and replaced by block 0).
-      auto tile_row = [&](int b, int t) -> int {
-        int blk = t < p.max_blocks ? __ldg(p.block_table + static_cast<size_t>(b) * p.max_blocks + t) : -1;
-        if (blk < 0 || blk >= p.n_pool_blocks) {
-          report(p.status, MLA_ERR_DEVICE_BOUNDS);
-          blk = 0;
-        }
-        return blk * kBlockRows;
-      };
       UnitIter iter = make_iter(p, g);
       Unit u;
       uint32_t it = 0;
@@ -330,7 +483,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int rs = it % kRopeSlots;
           if (ok && it >= kRopeSlots) ok = wait_bar(&bs->rope_empty[rs], ((it / kRopeSlots) - 1) & 1, p, bs, 2);
           if (!ok) break;
-          const int y = tile_row(u.b, t);
+          const int y = tile_row(p, u.b, t);
           uint8_t* st = smem + kOffStages + s * kStageBytes;
           mbar_arrive_expect_tx(&bs->full[s], kStageBytes + kRopeBoxBytes);
 #pragma unroll
@@ -351,7 +504,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // The whole warp runs this loop (operands stay warp-uniform); one elected
     // lane issues each batch of MMAs.
     {
-      const uint32_t idesc_s = idesc_bf16_f32(128, kTile, false, false);
+      const uint32_t idesc_s = Q8 ? idesc_f16_f32(128, kTile, false, false) : idesc_bf16_f32(128, kTile, false, false);
       UnitIter iter = make_iter(p, g);
       Unit u;
       uint32_t k = 0;  // S tiles issued (global); tile k sits in stage k % kStages
@@ -367,13 +520,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!(ok = wait_bar_warp(&bs->full[k % kStages], (k / kStages) & 1, p, bs, 4))) break;
           if (k >= 1 && !(ok = wait_counters(bs->n_s_read, k, p, bs, 5))) break;
           tc_fence_after();
-          const uint32_t st = smem_u32(smem + kOffStages + (k % kStages) * kStageBytes);
-          const uint32_t rope = smem_u32(smem + kOffRope + (k % kRopeSlots) * kRopeBoxBytes);
+          const uint32_t st = smem_u32(smem + kOffStages + (k % kStages) * L::kStageStride);
+          const uint32_t rope = Q8 ? st + kStageBytes : smem_u32(smem + kOffRope + (k % kRopeSlots) * kRopeBoxBytes);
           mma_score_tile_elect<kBoxBytes>(tmem + kTmemS, tmem + kTmemQ, tmem + kTmemQR,
                                           smem_desc(st, 16, 1024, kSwizzle128B),
                                           smem_desc(rope, 16, 512, kSwizzle64B), idesc_s);
           mma_commit_elect(&bs->s_full);
-          mma_commit_elect(&bs->rope_empty[k % kRopeSlots]);
+          if (!Q8) mma_commit_elect(&bs->rope_empty[k % kRopeSlots]);
         }
       }
       if (!ok) {
@@ -386,7 +539,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == kValueWarp) {
     // ------------------------------------------------------------ value MMA issuer
     {
-      const uint32_t idesc_o = idesc_bf16_f32(128, 256, false, true);
+      const uint32_t idesc_o = Q8 ? idesc_f16_f32(128, 256, false, true) : idesc_bf16_f32(128, 256, false, true);
       UnitIter iter = make_iter(p, g);
       Unit u;
       uint32_t k = 0;  // O MMAs issued (global)
@@ -396,7 +549,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // P(k) is in TMEM (and S(k) done, so the stage has landed)
           if (!(ok = wait_counters(bs->n_p_done, k + 1, p, bs, 6))) break;
           tc_fence_after();
-          const uint32_t st = smem_u32(smem + kOffStages + (k % kStages) * kStageBytes);
+          const uint32_t st = smem_u32(smem + kOffStages + (k % kStages) * L::kStageStride);
           mma_value_tile_elect<kTile / 16>(tmem + kTmemO, tmem + kTmemP, smem_desc(st, kBoxBytes, 1024, kSwizzle128B),
                                            idesc_o, t > u.ta ? 1u : 0u);
           mma_commit_elect(&bs->p_free);
@@ -430,6 +583,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint8_t* const inbox0 = smem + kOffInbox + rw * kXBlockBytes;
     uint8_t* const outbox = smem + kOffOutbox + rw * kXBlockBytes;
     const uint32_t peer_free0 = map_to_rank(smem_u32(&bs->inbox_free[0][rw]), peer);
+    // quantised cache: this warp ships its own blocks (warp 3 dequantises)
+    const uint32_t peer_inbox_rw = map_to_rank(smem_u32(inbox0), peer);
+    const uint32_t peer_xin_rw = map_to_rank(smem_u32(&bs->xin_full[0][rw]), peer);
     const int sw = (lane >> 1) & 3;
     const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
     UnitIter iter = make_iter(p, g);
@@ -459,15 +615,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         own[k] = mul_f32x2(make_float2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), scale2);
         h[k] = pack_half2(own[k].x, own[k].y);
       }
-      // the exchange warp's copy of the previous block has read the outbox
-      if (n_send >= 1 && !wait_counter(&bs->n_out_free[rw], n_send, p, bs, 10)) return false;
+      // the copy of the previous block has read the outbox
+      if constexpr (Q8) {
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+      } else {
+        if (n_send >= 1 && !wait_counter(&bs->n_out_free[rw], n_send, p, bs, 10)) return false;
+      }
       uint8_t* row = outbox + lane * 64;
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch)
         *reinterpret_cast<uint4*>(row + ((ch ^ sw) * 16)) = make_uint4(h[4 * ch], h[4 * ch + 1], h[4 * ch + 2], h[4 * ch + 3]);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) st_release_u32(&bs->n_out_ready[rw], n_send + 1);  // the exchange warp ships it
+      if constexpr (Q8) {
+        // into inbox slot n_send % 2 of the peer's same warp, once the peer has
+        // consumed what went there two blocks ago
+        const uint32_t slot = n_send & 1;
+        if (n_send >= 2 && !wait_bar(&bs->inbox_free[slot][rw], ((n_send >> 1) - 1) & 1, p, bs, 8, true))
+          return false;
+        if (lane == 0) {
+          bulk_copy_to_peer(peer_inbox_rw + slot * kXSlotBytes, outbox, kXBlockBytes, peer_xin_rw + slot * kBarSlot);
+          bulk_commit();
+        }
+      } else {
+        if (lane == 0) st_release_u32(&bs->n_out_ready[rw], n_send + 1);  // the exchange warp ships it
+      }
       ++n_send;
       return true;
     };
@@ -486,6 +659,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint4 w = __ldg(src + ch * 4 + j);
             v[4 * j] = w.x; v[4 * j + 1] = w.y; v[4 * j + 2] = w.z; v[4 * j + 3] = w.w;
           }
+          if constexpr (Q8) {  // the quantised path's MMAs take fp16 operands
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = bf16x2_to_f16x2(v[j]);
+          }
           tmem_st16(tmem + lane32 + kTmemQ + ch * 16, v);
         }
         const uint4* rsrc = reinterpret_cast<const uint4*>(p.q_lat + (static_cast<size_t>(u.n) * kHeads + r) * kWidth + 512 + 32 * c);
@@ -494,6 +671,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 4; ++j) {
           const uint4 w = __ldg(rsrc + j);
           v[4 * j] = w.x; v[4 * j + 1] = w.y; v[4 * j + 2] = w.z; v[4 * j + 3] = w.w;
+        }
+        if constexpr (Q8) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = bf16x2_to_f16x2(v[j]);
         }
         tmem_st16(tmem + lane32 + kTmemQR, v);
         tmem_st_wait();
@@ -564,7 +745,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const float2 x = add_f32x2(cur[k], (k & 1) ? nmb : nma);
           const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           if (k & 1) sb = add_f32x2(sb, e); else sa = add_f32x2(sa, e);
-          pk[k] = pack_bf16x2(e.x, e.y);
+          pk[k] = Q8 ? pack_half2(e.x, e.y) : pack_bf16x2(e.x, e.y);
         }
         la = (tt == 0) ? sa.x + sa.y : la * fa + (sa.x + sa.y);
         lb = (tt == 0) ? sb.x + sb.y : lb * fb + (sb.x + sb.y);
@@ -588,7 +769,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         // rows past the token's position may hold anything: zero them for the O MMA
         if (valid < kTile) {
-          uint8_t* st = smem + kOffStages + (n_p % kStages) * kStageBytes;
+          uint8_t* st = smem + kOffStages + (n_p % kStages) * L::kStageStride;
           for (int idx = tr; idx < (kTile - valid) * 32; idx += 32 * kRowWarps) {
             const int row = valid + (idx >> 5), box = (idx >> 3) & 3, ch = idx & 7;
             *reinterpret_cast<uint4*>(st + box * kBoxBytes + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
@@ -617,7 +798,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // O leaves TMEM in 32-column chunks staged through this warp's (idle)
       // outbox block (16 rows x 128 B fp32, 8-byte slots XOR-swizzled by row)
       // so that every global store covers whole row segments.
-      if (!(ok = wait_counter(&bs->n_out_free[rw], n_send, p, bs, 16))) break;  // no copy still reads the outbox
+      if constexpr (Q8) {  // no copy still reads the outbox
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+      } else {
+        if (!(ok = wait_counter(&bs->n_out_free[rw], n_send, p, bs, 16))) break;
+      }
       uint8_t* const stg = outbox;
       const int ra = lane >> 2;  // staging rows ra (head ha) and ra + 8 (head ha + 8)
       const size_t row0 = static_cast<size_t>(u.slot < 0 ? u.n : u.slot) * kHeads + q * 32 + hh * 16;
@@ -655,7 +841,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
     }
-  } else if (warp == kXchgWarp) {
+    if constexpr (Q8) {
+      // copies into the peer must have landed before the final cluster barrier
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
+    }
+  } else if (!Q8 && warp == kXchgWarp) {
     // ------------------------------------------------------------ exchange issuer
     // Lane rw ships softmax warp rw's fp16 partial block of every tile to the
     // same warp's inbox in the peer: once the block is written, and once the peer
@@ -925,11 +1116,23 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(
 }
 
 bool encode_pool_maps(const mla_handle* h, Maps* maps, const void* pool, long long rows) {
+  maps->codes = maps->scales = CUtensorMap{};
   return tensor_map_2d(h, &maps->latent, pool, kWidth, rows, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B) &&
          tensor_map_2d(h, &maps->rope, pool, kWidth, rows, 32, kTile, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// The quantised pool as [rows, 672] bytes: a CTA's 256 codes, its 8 scales
+// and its 64 bytes of k^R per row.
+bool encode_q8_pool_maps(const mla_handle* h, Maps* maps, const void* pool, long long rows) {
+  maps->latent = CUtensorMap{};
+  const auto u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  return tensor_map_2d(h, &maps->codes, pool, kQ8RowBytes, rows, 256, kTile, CU_TENSOR_MAP_SWIZZLE_NONE, u8) &&
+         tensor_map_2d(h, &maps->scales, pool, kQ8RowBytes, rows, 16, kTile, CU_TENSOR_MAP_SWIZZLE_NONE, u8) &&
+         tensor_map_2d(h, &maps->rope, pool, kQ8RowBytes, rows, 64, kTile, CU_TENSOR_MAP_SWIZZLE_64B, u8);
+}
+
 // plan -> decode -> combine, each allowed to launch while its predecessor finishes.
+template <bool Q8>
 cudaError_t launch_decode_kernels(const mla_handle* h, const Maps& maps, const Params& prm, int W, int n_tok,
                                   const int* seq_lens, const int* cu_q, int batch, int max_blocks, float* lse,
                                   int* status, cudaStream_t s) {
@@ -937,9 +1140,10 @@ cudaError_t launch_decode_kernels(const mla_handle* h, const Maps& maps, const P
                              const_cast<int*>(prm.prefix), const_cast<int2*>(prm.tok_info),
                              const_cast<int*>(prm.worker_plan), const_cast<int*>(prm.plan_flags), status);
   if (e != cudaSuccess) return e;
-  e = kernel_attrs_once(h, reinterpret_cast<const void*>(decode_tc_kernel), kSmemBytes, false);
+  constexpr int kSmemBytes = static_cast<int>(Layout<Q8>::kSmemBytes);
+  e = kernel_attrs_once(h, reinterpret_cast<const void*>(decode_tc_kernel<Q8>), kSmemBytes, false);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(decode_tc_kernel, dim3(2 * W), dim3(kThreads), kSmemBytes, s, 1, maps, prm);
+  e = launch_pdl(decode_tc_kernel<Q8>, dim3(2 * W), dim3(kThreads), kSmemBytes, s, 1, maps, prm);
   if (e != cudaSuccess) return e;
   return launch_pdl(combine_kernel, dim3(n_tok, kHeads), dim3(32 * kCombineWarps), 0, s, 1, static_cast<const int*>(prm.prefix),
                     prm.plan_flags, n_tok, W, static_cast<const float*>(prm.part_o), static_cast<const float*>(prm.part_lse), prm.o_lat,
@@ -988,11 +1192,12 @@ size_t decode_tc_workspace_bytes(const mla_handle* h, int n_tok, int num_workers
 cudaError_t launch_decode_tc(const mla_handle* h, const void* q_lat, const void* pool, int n_pool_blocks,
                              const int* block_table, int max_blocks, const int* seq_lens, const int* cu_q,
                              int batch, int n_tok, int num_workers, void* ws, size_t ws_bytes, void* o_lat,
-                             float* lse, cudaStream_t s) {
+                             float* lse, cudaStream_t s, bool q8) {
   const int W = resolve_workers(h, num_workers);
   Maps maps;
   const long long rows = static_cast<long long>(n_pool_blocks) * kBlockRows;
-  if (!encode_pool_maps(h, &maps, pool, rows)) return cudaErrorInvalidValue;
+  if (!(q8 ? encode_q8_pool_maps(h, &maps, pool, rows) : encode_pool_maps(h, &maps, pool, rows)))
+    return cudaErrorInvalidValue;
   Params prm;
   set_workspace(prm, static_cast<uint8_t*>(ws), ws_layout(static_cast<size_t>(n_tok), static_cast<size_t>(W)));
   prm.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
@@ -1010,7 +1215,8 @@ cudaError_t launch_decode_tc(const mla_handle* h, const void* q_lat, const void*
   prm.workers = W;
   prm.scale_log2 = h->dims.scale * kLog2e;
 
-  return launch_decode_kernels(h, maps, prm, W, n_tok, seq_lens, cu_q, batch, max_blocks, lse, h->status, s);
+  if (q8) return launch_decode_kernels<true>(h, maps, prm, W, n_tok, seq_lens, cu_q, batch, max_blocks, lse, h->status, s);
+  return launch_decode_kernels<false>(h, maps, prm, W, n_tok, seq_lens, cu_q, batch, max_blocks, lse, h->status, s);
 }
 
 
@@ -1103,7 +1309,7 @@ int launch_decode_tc_noalloc(const mla_handle* h, const void* q_lat, const void*
   prm.n_pool_blocks = n_pool_blocks;
   prm.workers = W;
   prm.scale_log2 = h->dims.scale * kLog2e;
-  return launch_decode_kernels(h, maps, prm, W, n_tok, seq_lens, cu_q, batch, max_blocks, lse, h->status, s) ==
+  return launch_decode_kernels<false>(h, maps, prm, W, n_tok, seq_lens, cu_q, batch, max_blocks, lse, h->status, s) ==
                  cudaSuccess
              ? 0
              : 2;

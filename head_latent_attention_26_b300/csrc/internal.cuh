@@ -168,7 +168,7 @@ cudaError_t launch_decode_tc(const mla_handle* h, const void* q_lat, const void*
                              int n_pool_blocks, const int* block_table, int max_blocks,
                              const int* seq_lens, const int* cu_q, int batch, int n_tok,
                              int num_workers, void* ws, size_t ws_bytes, void* o_lat, float* lse,
-                             cudaStream_t s);
+                             cudaStream_t s, bool q8 = false);
 // cuTensorMapEncodeTiled from the driver (looked up once); null if unavailable.
 PFN_cuTensorMapEncodeTiled_v12000 tma_encoder();
 // A 2-D tiled tensor map of a row-major [rows, cols] tensor with boxes of
@@ -198,6 +198,14 @@ cudaError_t launch_q_absorbed_tc(const mla_handle* h, const void* c_q, const voi
                                  const int* pos, int n_tok, void* q_lat, cudaStream_t s);
 cudaError_t launch_absorb_q_tc(const mla_handle* h, const void* q_c, const void* q_r, const int* pos, int n_tok,
                                const void* w_uk, void* q_lat, cudaStream_t s);
+cudaError_t launch_cache_rows_dense_tc(const mla_handle* h, const void* x, const void* w_dkr, const int* seq_idx,
+                                       const int* pos, int n_new, const int* block_table, int max_blocks, int batch,
+                                       int n_pool_blocks, void* rows, cudaStream_t s);
+// Quantised latent cache (rows of 672 bytes: int8 codes of c^KV, fp16 block
+// scales, bf16 k^R): quantise dense bf16 rows into the pool slots.
+cudaError_t launch_quantize_scatter_q8(const mla_handle* h, const void* rows, const int* seq_idx, const int* pos,
+                                       int n_new, const int* block_table, int max_blocks, int batch, void* pool,
+                                       int n_pool_blocks, cudaStream_t s);
 // Same kernels with their scratch in a fixed device array (no allocation).
 int launch_decode_tc_noalloc(const mla_handle* h, const void* q_lat, const void* pool, int n_pool_blocks,
                              const int* block_table, int max_blocks, const int* seq_lens, const int* cu_q,

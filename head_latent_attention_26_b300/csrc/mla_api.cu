@@ -214,6 +214,32 @@ mla_status mla_cache_append(mla_handle* h, const void* x, const void* w_dkr, con
   return MLA_OK;
 }
 
+// ---------------------------------------------------------------- a1, quantised cache
+size_t mla_cache_append_q8_workspace_bytes(const mla_handle* h, int n_new) {
+  if (!h || n_new < 0) return 0;
+  const size_t n = static_cast<size_t>(n_new) * (h->dims.d_c + h->dims.d_hr) * 2;
+  return (n + 255) & ~static_cast<size_t>(255);
+}
+
+mla_status mla_cache_append_q8(mla_handle* h, const void* x, const void* w_dkr, const int* seq_idx, const int* pos,
+                               int n_new, const int* block_table, int max_blocks, int batch, void* pool_q8,
+                               int n_pool_blocks, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!h || n_new < 0) return MLA_ERR_INVALID_ARG;
+  if (!h->tensor_path || !h->proj_tc) return MLA_ERR_UNSUPPORTED;
+  if (n_new == 0) return MLA_OK;
+  if (!x || !w_dkr || !pool_q8 || !aligned16(x) || !aligned16(w_dkr) || !aligned16(pool_q8))
+    return MLA_ERR_INVALID_ARG;
+  if (!seq_idx || !pos || !block_table || !aligned4(seq_idx) || !aligned4(pos) || !aligned4(block_table))
+    return MLA_ERR_INVALID_ARG;
+  if (max_blocks < 1 || batch < 1 || n_pool_blocks < 1) return MLA_ERR_INVALID_ARG;
+  if (!ws || !aligned16(ws) || ws_bytes < mla_cache_append_q8_workspace_bytes(h, n_new)) return MLA_ERR_WORKSPACE;
+  MLA_TRY_CUDA(mla::launch_cache_rows_dense_tc(h, x, w_dkr, seq_idx, pos, n_new, block_table, max_blocks, batch,
+                                               n_pool_blocks, ws, stream));
+  MLA_TRY_CUDA(mla::launch_quantize_scatter_q8(h, ws, seq_idx, pos, n_new, block_table, max_blocks, batch, pool_q8,
+                                               n_pool_blocks, stream));
+  return MLA_OK;
+}
+
 // ---------------------------------------------------------------- a2
 mla_status mla_absorb_q(mla_handle* h, const void* q_c, const void* q_r, const int* pos, int n_tok,
                         const void* w_uk, void* q_lat, cudaStream_t stream) {
@@ -287,6 +313,25 @@ mla_status mla_decode(mla_handle* h, const void* q_lat, const void* pool, int n_
     MLA_TRY_CUDA(mla::launch_decode_simt(h, q_lat, pool, n_pool_blocks, block_table, max_blocks, seq_lens,
                                          cu_q, batch, n_tok, o_lat, lse, stream));
   }
+  return MLA_OK;
+}
+
+mla_status mla_decode_q8(mla_handle* h, const void* q_lat, const void* pool_q8, int n_pool_blocks,
+                         const int* block_table, int max_blocks, const int* seq_lens, const int* cu_q, int batch,
+                         int n_tok, int num_workers, void* ws, size_t ws_bytes, void* o_lat, float* lse,
+                         cudaStream_t stream) {
+  if (!h || n_tok < 0 || batch < 0 || num_workers < 0) return MLA_ERR_INVALID_ARG;
+  if (!h->tensor_path) return MLA_ERR_UNSUPPORTED;
+  if (n_tok == 0) return MLA_OK;
+  if (batch < 1 || max_blocks < 1 || n_pool_blocks < 1) return MLA_ERR_INVALID_ARG;
+  for (const void* p : {q_lat, pool_q8, static_cast<const void*>(o_lat), static_cast<const void*>(lse)})
+    if (!p || !aligned16(p)) return MLA_ERR_INVALID_ARG;
+  for (const int* p : {block_table, seq_lens, cu_q})
+    if (!p || !aligned4(p)) return MLA_ERR_INVALID_ARG;
+  const size_t need = mla_decode_workspace_bytes(h, n_tok, num_workers);
+  if (!ws || !aligned16(ws) || ws_bytes < need) return MLA_ERR_WORKSPACE;
+  MLA_TRY_CUDA(mla::launch_decode_tc(h, q_lat, pool_q8, n_pool_blocks, block_table, max_blocks, seq_lens, cu_q,
+                                     batch, n_tok, num_workers, ws, ws_bytes, o_lat, lse, stream, true));
   return MLA_OK;
 }
 

@@ -77,6 +77,7 @@ struct ProjParams {
   const int* pos;
   const int* block_table;
   int max_blocks, batch, n_pool_blocks, max_pos, d_c, d_hr, width, block;
+  int dense;  // append: row n of the tile goes to row n of `pool` (a dense [n_new, width] buffer)
   __nv_bfloat16* pool;
   const float* rope_cos;
   const float* rope_sin;
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         } else {
           const int blk = __ldg(p.block_table + static_cast<size_t>(b) * p.max_blocks + tp / p.block);
           if (blk < 0 || blk >= p.n_pool_blocks) report(p.status, MLA_ERR_DEVICE_BOUNDS);
-          else slot = blk * p.block + tp % p.block;
+          else slot = p.dense ? n : blk * p.block + tp % p.block;
         }
       }
       ss->slot[j] = slot;
@@ -613,6 +614,35 @@ cudaError_t launch_cache_append_tc(const mla_handle* h, const void* x, const voi
   p.batch = batch;
   p.n_pool_blocks = n_pool_blocks;
   p.pool = static_cast<__nv_bfloat16*>(pool);
+  maps.w2 = maps.w;
+  p.seg1_tiles = 1 << 30;
+  return launch_proj<kModeAppend, 1>(h, maps, p, pick_split(h, o_tiles, n_new, p.k_blocks), o_tiles, s);
+}
+
+// The cache rows of the new tokens, [n_new, d_c + d_hr] bf16 in token order
+// (the append epilogue with the block-table scatter replaced by row n).  The
+// block table is still read to check each token's sequence and position.
+cudaError_t launch_cache_rows_dense_tc(const mla_handle* h, const void* x, const void* w_dkr, const int* seq_idx,
+                                       const int* pos, int n_new, const int* block_table, int max_blocks, int batch,
+                                       int n_pool_blocks, void* rows, cudaStream_t s) {
+  const mla_dims& d = h->dims;
+  const int width = d.d_c + d.d_hr;
+  ProjMaps maps;
+  if (!encode_bf16_2d(h, &maps.w, w_dkr, d.d_model, width, kBK, kBM) ||
+      !encode_bf16_2d(h, &maps.x, x, d.d_model, n_new, kBK, token_tile(n_new)))
+    return cudaErrorInvalidValue;
+  ProjParams p = base_params(h, n_new);
+  const int o_tiles = (width + kBM - 1) / kBM;
+  p.out = width;
+  p.k_blocks = (d.d_model + kBK - 1) / kBK;
+  p.seq_idx = seq_idx;
+  p.pos = pos;
+  p.block_table = block_table;
+  p.max_blocks = max_blocks;
+  p.batch = batch;
+  p.n_pool_blocks = n_pool_blocks;
+  p.pool = static_cast<__nv_bfloat16*>(rows);
+  p.dense = 1;
   maps.w2 = maps.w;
   p.seg1_tiles = 1 << 30;
   return launch_proj<kModeAppend, 1>(h, maps, p, pick_split(h, o_tiles, n_new, p.k_blocks), o_tiles, s);

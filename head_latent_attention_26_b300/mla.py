@@ -57,12 +57,15 @@ _SIGS = {
     "mla_q_proj_workspace_bytes": (SZ, [P, I]),
     "mla_q_proj": (I, [P, P, P, P, P, I, P, P, P, SZ, P]),
     "mla_cache_append": (I, [P, P, P, P, P, I, P, I, I, P, I, P]),
+    "mla_cache_append_q8_workspace_bytes": (SZ, [P, I]),
+    "mla_cache_append_q8": (I, [P, P, P, P, P, I, P, I, I, P, I, P, SZ, P]),
     "mla_absorb_q": (I, [P, P, P, P, I, P, P, P]),
     "mla_absorb_weights": (I, [P, P, P, P, P]),
     "mla_q_proj_absorbed": (I, [P, P, P, P, P, P, I, P, P, SZ, P]),
     "mla_decode_workspace_bytes": (SZ, [P, I, I]),
     "mla_decode": (I, [P, P, P, I, P, I, P, P, I, I, I, P, SZ, P, P, P]),
     "mla_decode_noalloc": (I, [P, P, P, I, P, I, P, P, I, I, I, P, P, P]),
+    "mla_decode_q8": (I, [P, P, P, I, P, I, P, P, I, I, I, P, SZ, P, P, P]),
     "mla_out_workspace_bytes": (SZ, [P, I]),
     "mla_out": (I, [P, P, P, P, I, P, P, SZ, P]),
     "mla_check_device_status": (I, [P, P]),
@@ -190,6 +193,17 @@ class MLA:
                                          _ptr(pool), pool.shape[0], P(_stream())), "mla_cache_append")
         return pool
 
+    def cache_append_q8(self, x, W_dkr, seq_idx, pos, block_table, pool_q8):
+        """mla_cache_append_q8: the new tokens' rows, quantised, into a
+        [n_blocks, block, 672] uint8 pool."""
+        n = x.shape[0]
+        ws = self.workspace("append_q8", self.lib.mla_cache_append_q8_workspace_bytes(self.h, n))
+        _check(self.lib.mla_cache_append_q8(self.h, _ptr(x), _ptr(W_dkr), _ptr(seq_idx), _ptr(pos), n,
+                                            _ptr(block_table), block_table.shape[1], block_table.shape[0],
+                                            _ptr(pool_q8), pool_q8.shape[0], _ptr(ws), ws.numel(), P(_stream())),
+               "mla_cache_append_q8")
+        return pool_q8
+
     def absorb_q(self, q_c, q_r, pos, W_uk, q_lat=None):
         d, n = self.dims, q_c.shape[0]
         q_lat = torch.empty(n, d.n_h, d.width, dtype=self.dtype, device=q_c.device) if q_lat is None else q_lat
@@ -231,6 +245,21 @@ class MLA:
                                    block_table.shape[1], _ptr(seq_lens), _ptr(cu_q), seq_lens.shape[0], n,
                                    num_workers, _ptr(ws), ws.numel(), _ptr(o_lat), _ptr(lse), P(_stream())),
                "mla_decode")
+        return o_lat, lse
+
+    def decode_q8(self, q_lat, pool_q8, block_table, seq_lens, cu_q, num_workers: int = 0, o_lat=None, lse=None,
+                  ws=None):
+        """mla_decode_q8: the attention over a quantised cache pool
+        ([n_blocks, block, 672] uint8)."""
+        d, n = self.dims, q_lat.shape[0]
+        o_lat = torch.empty(n, d.n_h, d.d_c, dtype=self.dtype, device=q_lat.device) if o_lat is None else o_lat
+        lse = torch.empty(n, d.n_h, dtype=torch.float32, device=q_lat.device) if lse is None else lse
+        if ws is None:
+            ws = self.workspace("decode", self.decode_workspace_bytes(n, num_workers))
+        _check(self.lib.mla_decode_q8(self.h, _ptr(q_lat), _ptr(pool_q8), pool_q8.shape[0], _ptr(block_table),
+                                      block_table.shape[1], _ptr(seq_lens), _ptr(cu_q), seq_lens.shape[0], n,
+                                      num_workers, _ptr(ws), ws.numel(), _ptr(o_lat), _ptr(lse), P(_stream())),
+               "mla_decode_q8")
         return o_lat, lse
 
     def decode_noalloc(self, q_lat, pool, block_table, seq_lens, cu_q, num_workers: int = 0, o_lat=None,

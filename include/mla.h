@@ -124,6 +124,28 @@ mla_status mla_cache_append(mla_handle* h, const void* x, const void* w_dkr, con
                             const int* pos, int n_new, const int* block_table, int max_blocks,
                             int batch, void* pool, int n_pool_blocks, cudaStream_t stream);
 
+/* ---- a1 with the quantised latent cache -------------------------------------
+ * [0h-n0] "量子化との組み合わせ": c^KV can further be stored with KV-cache
+ * quantisation of the Q8_0 kind.  Each cached row becomes 672 bytes:
+ *   bytes [0, 512)    int8 codes of c^KV, value j in byte j
+ *   bytes [512, 544)  16 fp16 scales, scale b for values [32b, 32b+32)
+ *   bytes [544, 672)  k^R, 64 bf16 values (stored after the rotation)
+ * Value j stands for code_j * scale_(j/32).  The row quantised is the bf16
+ * row mla_cache_append would store; per 32-value run, scale = fp16(max|x| /
+ * 127) and code = x / scale rounded to nearest with ties away from zero (both
+ * divisions in fp32, correctly rounded), 0 when the run is all zero.
+ *   x, w_dkr, seq_idx, pos, block_table, max_blocks, batch: as in
+ *   mla_cache_append
+ *   pool_q8 [n_pool_blocks, block, 672] bytes (written), 16-byte aligned
+ *   ws: mla_cache_append_q8_workspace_bytes(h, n_new) bytes (the bf16 rows)
+ * Tensor-path sizes only (n_h = 128, d_c = 512, d_hr = 64, block = 64, bf16);
+ * others return MLA_ERR_UNSUPPORTED.  Bounds errors as in mla_cache_append. */
+size_t mla_cache_append_q8_workspace_bytes(const mla_handle* h, int n_new);
+mla_status mla_cache_append_q8(mla_handle* h, const void* x, const void* w_dkr, const int* seq_idx,
+                               const int* pos, int n_new, const int* block_table, int max_blocks,
+                               int batch, void* pool_q8, int n_pool_blocks, void* ws, size_t ws_bytes,
+                               cudaStream_t stream);
+
 /* ---- a2: query absorption --------------------------------------------------
  * [0h-n0] "行列吸収トリック": q~_i = W^UK_i^T q^C_i (d_c), and q^R_i rotated at
  * the token's position ([qiita] "RoPE の扱い").
@@ -184,6 +206,19 @@ mla_status mla_decode(mla_handle* h, const void* q_lat, const void* pool, int n_
                       const int* block_table, int max_blocks, const int* seq_lens,
                       const int* cu_q, int batch, int n_tok, int num_workers, void* ws,
                       size_t ws_bytes, void* o_lat, float* lse, cudaStream_t stream);
+
+/* ---- a3 + a4 over the quantised latent cache -------------------------------
+ * The attention of mla_decode with the cache rows of mla_cache_append_q8
+ * ([0h-n0] "量子化との組み合わせ"): row j stands for [code_j * scale_(j/32) ;
+ * k^R], and each value is rounded once to bf16 on chip before the MMAs.  The
+ * cache stream is 672 bytes per row instead of 1152.
+ *   pool_q8 [n_pool_blocks, block, 672] bytes; every other argument, the
+ *   workspace (mla_decode_workspace_bytes) and the outputs as in mla_decode.
+ * Tensor-path sizes only; others return MLA_ERR_UNSUPPORTED. */
+mla_status mla_decode_q8(mla_handle* h, const void* q_lat, const void* pool_q8, int n_pool_blocks,
+                         const int* block_table, int max_blocks, const int* seq_lens, const int* cu_q,
+                         int batch, int n_tok, int num_workers, void* ws, size_t ws_bytes, void* o_lat,
+                         float* lse, cudaStream_t stream);
 
 /* ---- decode without a workspace argument ------------------------------------
  * The pages have no counterpart to this call; it is a convenience of this
