@@ -8,6 +8,10 @@ permutation of the pool):
   b1_t4096     B=1, T=4096
   b1_t131072   B=1, T=131072 (128K context), 1% of the cached rows scaled by 8
   ragged_b128  B=128, T_b ~ U[512, 16384], 1 or 2 new tokens per sequence
+  b64_t4096_q8 b64_t4096 over the quantised latent cache (int8 codes of c^KV
+               with an fp16 scale per 32 values, bf16 k^R: 672 B per row)
+  prefill_p4096  a P=4096-token prompt: query projection, cache rows, and
+               causal attention over the expanded keys and values
 
 One step = the whole path for the step's new tokens: query projection, cache
 append, W^UK absorption, latent attention (+ split combine), W^UV / W^O output.
@@ -74,7 +78,12 @@ WORKLOADS = {
     "b1_t4096": dict(kind="uniform", B=1, T=4096, hot=0.0),
     "b1_t131072": dict(kind="uniform", B=1, T=131072, hot=0.01),
     "ragged_b128": dict(kind="ragged", B=128, lo=512, hi=16384, hot=0.0),
+    # the headline step over the quantised latent cache (672-byte rows)
+    "b64_t4096_q8": dict(kind="uniform", B=64, T=4096, hot=0.0, q8=True),
+    # a 4096-token prompt through the expanded-K/V prefill
+    "prefill_p4096": dict(kind="prefill", P=4096),
 }
+Q8_ROW_BYTES = 672
 
 
 def _peaks():
@@ -295,6 +304,27 @@ def make_workload(lens, qc, hot: float, device="cuda"):
     return d, W, W_dkr, table, pool, inp
 
 
+def quantise_pool_q8(pool):
+    """Input set-up for the quantised-cache workload, in plain torch: each
+    bf16 row [c (512) ; k^R (64)] as 672 bytes -- per run of 32 values of c an
+    fp16 scale d = max|x| / 127 and int8 codes round(x / d) (nearest, ties
+    away from zero), then the bf16 k^R bytes."""
+    d = synth.V2
+    flat = pool.view(-1, d.width)
+    out = torch.empty(flat.shape[0], Q8_ROW_BYTES, dtype=torch.uint8, device=pool.device)
+    for i in range(0, flat.shape[0], 65536):
+        j = min(flat.shape[0], i + 65536)
+        c = flat[i:j, :d.d_c].float().view(j - i, d.d_c // 32, 32)
+        sc = (c.abs().amax(-1) / 127.0).half()
+        sf = sc.float().unsqueeze(-1)
+        q = torch.where(sf > 0, c / torch.where(sf > 0, sf, torch.ones_like(sf)), torch.zeros_like(c))
+        code = (torch.sign(q) * torch.floor(q.abs() + 0.5)).clamp(-127, 127).to(torch.int8)
+        out[i:j, :d.d_c] = code.view(j - i, d.d_c).view(torch.uint8)
+        out[i:j, d.d_c:d.d_c + 32] = sc.contiguous().view(torch.uint8).view(j - i, 32)
+        out[i:j, d.d_c + 32:] = flat[i:j, d.d_c:].contiguous().view(torch.uint8)
+    return out.view(pool.shape[0], pool.shape[1], Q8_ROW_BYTES)
+
+
 def algorithmic(B: int, T: int, d=synth.V2):
     """Bytes and flops the decode kernel must move / do for B sequences of T
     rows with one query token each (one launch)."""
@@ -305,12 +335,13 @@ def algorithmic(B: int, T: int, d=synth.V2):
     return cache, cache + q + out, flops
 
 
-def algorithmic_tokens(visible, d=synth.V2):
+def algorithmic_tokens(visible, d=synth.V2, row_bytes=None):
     """The same for query tokens that see `visible[n]` cached rows each: per
-    token its rows of cache, its latent query read, its o_lat / lse written."""
+    token its rows of cache (row_bytes each; default the bf16 row), its latent
+    query read, its o_lat / lse written."""
     rows = int(sum(visible))
     n = len(visible)
-    cache = rows * d.width * 2
+    cache = rows * (row_bytes if row_bytes else d.width * 2)
     total = cache + n * d.n_h * d.width * 2 + n * d.n_h * d.d_c * 2 + n * d.n_h * 4
     flops = d.n_h * rows * (2 * d.width + 2 * d.d_c)
     return cache, total, flops
@@ -343,53 +374,11 @@ def _capture_chunks(step, K: int, events: bool, chunk: int = 256):
     return graphs, pairs
 
 
-def run_ours(args):
-    ws, rank = _dist()
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    _init_dist(ws, "nccl")
-    from head_latent_attention_26_b300 import build
-    build.build()
-    from head_latent_attention_26_b300 import mla
-    lens, qc, hot, desc = workload_shape(args.workload, args.batch, args.seq_len)
-    d, W, W_dkr, table, pool, inp = make_workload(lens, qc, hot)
-    B, N = len(lens), int(sum(qc))
-    m = mla.MLA(d, max(lens) + 64, torch.bfloat16)
-    assert m.tensor_path
-    bufs = {
-        "q_c": torch.empty(N, d.n_h, d.d_h, dtype=torch.bfloat16, device="cuda"),
-        "q_r": torch.empty(N, d.n_h, d.d_hr, dtype=torch.bfloat16, device="cuda"),
-        "q_lat": torch.empty(N, d.n_h, d.width, dtype=torch.bfloat16, device="cuda"),
-        "o_lat": torch.empty(N, d.n_h, d.d_c, dtype=torch.bfloat16, device="cuda"),
-        "lse": torch.empty(N, d.n_h, dtype=torch.float32, device="cuda"),
-        "u": torch.empty(N, d.d_model, dtype=torch.bfloat16, device="cuda"),
-    }
-    ws_dec = m.workspace("decode", m.decode_workspace_bytes(N, args.num_workers))
-    x_dev = torch.empty_like(inp["x"])
-    x_dev.copy_(inp["x"])
-
-    def step(pairs=None, x=None):
-        x = x_dev if x is None else x
-        if pairs is not None:
-            ea = torch.cuda.Event(enable_timing=True, external=True)
-            ea.record()
-        m.q_proj(x, W["W_dq"], W["W_uq"], W["W_qr"], bufs["q_c"], bufs["q_r"])
-        m.cache_append(x, W_dkr, inp["seq_idx"], inp["pos"], table, pool)
-        if pairs is not None:
-            eb = torch.cuda.Event(enable_timing=True, external=True)
-            eb.record()
-        m.absorb_q(bufs["q_c"], bufs["q_r"], inp["pos"], W["W_uk"], bufs["q_lat"])
-        if pairs is not None:
-            e0 = torch.cuda.Event(enable_timing=True, external=True)
-            e0.record()
-        m.decode(bufs["q_lat"], pool, table, inp["seq_lens"], inp["cu_q"], args.num_workers, bufs["o_lat"],
-                 bufs["lse"], ws_dec)
-        if pairs is not None:
-            e1 = torch.cuda.Event(enable_timing=True, external=True)
-            e1.record()
-            pairs.append((ea, eb, e0, e1))
-        m.out(bufs["o_lat"], W["W_uv"], W["W_o"], bufs["u"])
-
+def _measure(m, step, e2e_step, args, ws: int, local: int) -> dict:
+    """Times args.steps steps: captured as CUDA graphs with event nodes
+    (step(pairs) appends its events), again without event nodes, and end to
+    end (e2e_step: host copies in and out around a step, one graph replay per
+    step from the host loop); SM clocks are sampled inside the timed regions."""
     # eager calls first: the library sets kernel attributes, encodes tensor
     # maps and sizes its launches once; the captured calls then do no host work
     step()
@@ -415,10 +404,6 @@ def run_ours(args):
     clocks.mark(w0, time.time())
     m.check()
     ms = t0.elapsed_time(t1) / args.steps
-    # per timed step: the q_proj + append part, and the decode call (plan +
-    # decode + combine), each between event nodes on the step's stream
-    app_ms = sum(ea.elapsed_time(eb) for ea, eb, _, _ in pairs) / len(pairs)
-    dec_ms = sum(e0.elapsed_time(e1) for _, _, e0, e1 in pairs) / len(pairs)
     region_s = ms * args.steps * 1e-3
 
     # the same steps without event nodes (nothing between the kernels but the
@@ -435,6 +420,79 @@ def run_ours(args):
     ms_plain = t0.elapsed_time(t1) / args.steps
     del graphs_plain
 
+    g_e2e, _ = _capture(e2e_step, 1, events=False)
+    for _ in range(3):
+        g_e2e.replay()
+    _barrier(ws)
+    w0 = time.time()
+    t0.record()
+    for _ in range(args.steps):
+        g_e2e.replay()
+    t1.record()
+    _barrier(ws)
+    clocks.mark(w0, time.time())
+    e2e_ms = t0.elapsed_time(t1) / args.steps
+    clk = clocks.stop()
+    m.check()
+    del graphs, warm, g_e2e
+    return dict(ms=ms, ms_plain=ms_plain, pairs=pairs, e2e_ms=e2e_ms, clk=clk, region_s=region_s)
+
+
+def run_ours(args):
+    ws, rank = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    _init_dist(ws, "nccl")
+    from head_latent_attention_26_b300 import build
+    build.build()
+    from head_latent_attention_26_b300 import mla
+    lens, qc, hot, desc = workload_shape(args.workload, args.batch, args.seq_len)
+    d, W, W_dkr, table, pool, inp = make_workload(lens, qc, hot)
+    B, N = len(lens), int(sum(qc))
+    q8 = WORKLOADS[args.workload].get("q8", False)
+    if q8:
+        pool = quantise_pool_q8(pool)
+        desc += "; quantised latent cache (int8 codes of c^KV, fp16 scale per 32 values, bf16 k^R: 672 B per row)"
+    m = mla.MLA(d, max(lens) + 64, torch.bfloat16)
+    assert m.tensor_path
+    bufs = {
+        "q_c": torch.empty(N, d.n_h, d.d_h, dtype=torch.bfloat16, device="cuda"),
+        "q_r": torch.empty(N, d.n_h, d.d_hr, dtype=torch.bfloat16, device="cuda"),
+        "q_lat": torch.empty(N, d.n_h, d.width, dtype=torch.bfloat16, device="cuda"),
+        "o_lat": torch.empty(N, d.n_h, d.d_c, dtype=torch.bfloat16, device="cuda"),
+        "lse": torch.empty(N, d.n_h, dtype=torch.float32, device="cuda"),
+        "u": torch.empty(N, d.d_model, dtype=torch.bfloat16, device="cuda"),
+    }
+    ws_dec = m.workspace("decode", m.decode_workspace_bytes(N, args.num_workers))
+    x_dev = torch.empty_like(inp["x"])
+    x_dev.copy_(inp["x"])
+
+    def step(pairs=None, x=None):
+        x = x_dev if x is None else x
+        if pairs is not None:
+            ea = torch.cuda.Event(enable_timing=True, external=True)
+            ea.record()
+        m.q_proj(x, W["W_dq"], W["W_uq"], W["W_qr"], bufs["q_c"], bufs["q_r"])
+        if q8:
+            m.cache_append_q8(x, W_dkr, inp["seq_idx"], inp["pos"], table, pool)
+        else:
+            m.cache_append(x, W_dkr, inp["seq_idx"], inp["pos"], table, pool)
+        if pairs is not None:
+            eb = torch.cuda.Event(enable_timing=True, external=True)
+            eb.record()
+        m.absorb_q(bufs["q_c"], bufs["q_r"], inp["pos"], W["W_uk"], bufs["q_lat"])
+        if pairs is not None:
+            e0 = torch.cuda.Event(enable_timing=True, external=True)
+            e0.record()
+        dec = m.decode_q8 if q8 else m.decode
+        dec(bufs["q_lat"], pool, table, inp["seq_lens"], inp["cu_q"], args.num_workers, bufs["o_lat"], bufs["lse"],
+            ws_dec)
+        if pairs is not None:
+            e1 = torch.cuda.Event(enable_timing=True, external=True)
+            e1.record()
+            pairs.append((ea, eb, e0, e1))
+        m.out(bufs["o_lat"], W["W_uv"], W["W_o"], bufs["u"])
+
     # end to end through the public API with host buffers: every step copies
     # its inputs from pinned host memory, runs, and copies u back -- all inside
     # the timed region (one graph replay per step, launched from the host loop)
@@ -450,24 +508,17 @@ def run_ours(args):
         step()
         h_u.copy_(bufs["u"], non_blocking=True)
 
-    g_e2e, _ = _capture(e2e_step, 1, events=False)
-    for _ in range(3):
-        g_e2e.replay()
-    _barrier(ws)
-    w0 = time.time()
-    t0.record()
-    for _ in range(args.steps):
-        g_e2e.replay()
-    t1.record()
-    _barrier(ws)
-    clocks.mark(w0, time.time())
-    e2e_ms = t0.elapsed_time(t1) / args.steps
-    clk = clocks.stop()
-    m.check()
-    # kernels per step: q_proj 2 (W^DQ; W^UQ with W^QR), append 1, absorb 1,
-    # decode 3 (plan, attention, combine), out 2 (W^UV, W^O)
-    n_launch = 9
-    del graphs, warm, g_e2e
+    res_t = _measure(m, step, e2e_step, args, ws, local)
+    ms, ms_plain, pairs, e2e_ms, clk, region_s = (res_t[k] for k in ("ms", "ms_plain", "pairs", "e2e_ms", "clk",
+                                                                       "region_s"))
+    # per timed step: the q_proj + append part, and the decode call (plan +
+    # decode + combine), each between event nodes on the step's stream
+    app_ms = sum(ea.elapsed_time(eb) for ea, eb, _, _ in pairs) / len(pairs)
+    dec_ms = sum(e0.elapsed_time(e1) for _, _, e0, e1 in pairs) / len(pairs)
+    # kernels per step: q_proj 2 (W^DQ; W^UQ with W^QR), append 1 (quantised
+    # cache: 2, the rows then their codes), absorb 1, decode 3 (plan,
+    # attention, combine), out 2 (W^UV, W^O)
+    n_launch = 10 if q8 else 9
 
     ms, ms_plain, dec_ms, app_ms, e2e_ms = _max_over_ranks([ms, ms_plain, dec_ms, app_ms, e2e_ms], ws)
     if rank != 0:
@@ -478,7 +529,7 @@ def run_ours(args):
     for b in range(B):
         for k in range(int(qc[b])):
             visible.append(int(lens[b]) - int(qc[b]) + k + 1)
-    cache_b, dec_bytes, flops = algorithmic_tokens(visible, d)
+    cache_b, dec_bytes, flops = algorithmic_tokens(visible, d, Q8_ROW_BYTES if q8 else None)
     t = dec_ms * 1e-3
     gbs = dec_bytes / t / 1e9
     tflops = flops / t / 1e12
@@ -490,8 +541,10 @@ def run_ours(args):
                 "frac": round(tflops / tf_peak, 4)}
     else:
         roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4)}
-    traffic = args.traffic if args.traffic is not None else _profiled_traffic(B, lens[0] if len(set(lens)) == 1 else -1)
-    roof.update(kernel="decode_tc_kernel (+plan, combine)", peak_source=f"{src} (MEASURED_PEAKS.json), "
+    traffic = args.traffic if args.traffic is not None else (
+        None if q8 else _profiled_traffic(B, lens[0] if len(set(lens)) == 1 else -1))
+    roof.update(kernel="decode_tc_kernel<quantised> (+plan, combine)" if q8 else "decode_tc_kernel (+plan, combine)",
+                peak_source=f"{src} (MEASURED_PEAKS.json), "
                 f"tensor peak {tc_kind} (timed region {region_s * 1e3:.1f} ms)",
                 traffic=traffic,
                 other={"hbm": {"achieved_gbs": round(gbs, 1), "peak": hbm, "frac": round(gbs / hbm, 4)},
@@ -540,6 +593,127 @@ def run_ours(args):
                               "pool_bytes": pool.numel() * 2}
     if not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(lens, qc, args.workload, budget_s=args.cpu_budget)
+    return res
+
+
+def prefill_work(P: int, d=synth.V2):
+    """Algorithmic flops and bytes of one prefill call for a P-token prompt
+    (positions 0..P-1): the K^C and V expansion (two products of P x d_c by
+    d_c x n_h d_h) and the causal attention (per head sum_t (t+1) keys, each
+    a 192-wide score and a 128-wide weighted sum); bytes = the rows, query
+    parts and the two weights read, K^C and V written and read once, o and
+    lse written."""
+    hd = d.n_h * d.d_h
+    f_exp = 2 * 2 * P * hd * d.d_c
+    f_att = d.n_h * (P * (P + 1) // 2) * (2 * (d.d_h + d.d_hr) + 2 * d.d_h)
+    byt = (P * d.width * 2 + P * hd * 2 + P * d.n_h * d.d_hr * 2 + 2 * hd * d.d_c * 2
+           + 2 * (2 * P * hd * 2) + P * hd * 2 + P * d.n_h * 4)
+    return f_exp + f_att, byt, f_exp, f_att
+
+
+def run_prefill(args):
+    """A P-token prompt: mla_q_proj, mla_cache_append (rows in position
+    order), mla_prefill (K^C / V expansion + causal attention); events around
+    the prefill call."""
+    ws, rank = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    _init_dist(ws, "nccl")
+    from head_latent_attention_26_b300 import build
+    build.build()
+    from head_latent_attention_26_b300 import mla
+    P = args.seq_len if args.seq_len is not None else WORKLOADS[args.workload]["P"]
+    d = synth.V2
+    W = synth.weights(d, SEED, device="cuda")
+    W_dkr = torch.cat([W["W_dkv"], W["W_kr"]], dim=0).contiguous()
+    x_dev = synth.hidden(P, d, SEED, name="h_prompt", device="cuda")
+    m = mla.MLA(d, P + 64, torch.bfloat16)
+    assert m.tensor_path
+    n_blocks = (P + d.block - 1) // d.block
+    table = torch.arange(n_blocks, dtype=torch.int32, device="cuda").view(1, -1)
+    pool = torch.empty(n_blocks, d.block, d.width, dtype=torch.bfloat16, device="cuda")
+    rows = pool.view(-1, d.width)[:P]
+    seq_idx = torch.zeros(P, dtype=torch.int32, device="cuda")
+    pos = torch.arange(P, dtype=torch.int32, device="cuda")
+    q_c = torch.empty(P, d.n_h, d.d_h, dtype=torch.bfloat16, device="cuda")
+    q_r = torch.empty(P, d.n_h, d.d_hr, dtype=torch.bfloat16, device="cuda")
+    o = torch.empty(P, d.n_h, d.d_h, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(P, d.n_h, dtype=torch.float32, device="cuda")
+
+    def step(pairs=None):
+        m.q_proj(x_dev, W["W_dq"], W["W_uq"], W["W_qr"], q_c, q_r)
+        m.cache_append(x_dev, W_dkr, seq_idx, pos, table, pool)
+        if pairs is not None:
+            e0 = torch.cuda.Event(enable_timing=True, external=True)
+            e0.record()
+        m.prefill(rows, q_c, q_r, W["W_uk"], W["W_uv"], o, lse)
+        if pairs is not None:
+            e1 = torch.cuda.Event(enable_timing=True, external=True)
+            e1.record()
+            pairs.append((e0, e1))
+
+    h_x = x_dev.cpu().pin_memory()
+    h_o = torch.empty(P, d.n_h, d.d_h, dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step(_=None):
+        x_dev.copy_(h_x, non_blocking=True)
+        step()
+        h_o.copy_(o, non_blocking=True)
+
+    res_t = _measure(m, step, e2e_step, args, ws, local)
+    pre_ms = sum(e0.elapsed_time(e1) for e0, e1 in res_t["pairs"]) / len(res_t["pairs"])
+    ms, ms_plain, pre_ms, e2e_ms = _max_over_ranks([res_t["ms"], res_t["ms_plain"], pre_ms, res_t["e2e_ms"]], ws)
+    if rank != 0:
+        return None
+    hbm, tf_burst, tf_sus, src = _peaks()
+    flops, byt, f_exp, f_att = prefill_work(P, d)
+    t = pre_ms * 1e-3
+    bound, t_roof, tc_kind = roofline_choice(byt / (hbm * 1e9), flops / (tf_burst * 1e12), flops / (tf_sus * 1e12),
+                                             res_t["region_s"])
+    tf_peak = tf_sus if tc_kind == "sustained" else tf_burst
+    if bound == "tensor":
+        roof = {"bound": "tensor", "achieved": round(flops / t / 1e12, 1), "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": round(flops / t / 1e12 / tf_peak, 4)}
+    else:
+        roof = {"bound": "hbm", "achieved": round(byt / t / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(byt / t / 1e9 / hbm, 4)}
+    roof.update(kernel="mla_prefill (expansion GEMM + prefill_attn_kernel)", traffic=None,
+                peak_source=f"{src} (MEASURED_PEAKS.json), tensor peak {tc_kind} (fp16 operands, the bf16 rate)",
+                algorithmic_flops=flops, algorithmic_bytes=byt, expansion_flops=f_exp, attention_flops=f_att,
+                prefill_us=round(pre_ms * 1e3, 2))
+    n = ws
+    res = {
+        "metric": METRIC,
+        "value": round(_job_rate(P, n, ms), 1),
+        "unit": "tokens/s",
+        "n_gpus": n,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"MLA prefill, DeepSeek-V2 layer, one prompt of P={P} tokens (positions 0..P-1): "
+                               "query projection, cache rows, K^C / V expansion and causal attention",
+                   "batch": 1, "tokens_per_step": P, "seq_len": P,
+                   "parallelism": f"replicas x{n}" if n > 1 else "single GPU",
+                   "l2": "no flush: the step writes and reads the expanded K^C and V "
+                         f"({2 * P * d.n_h * d.d_h * 2 / 1e6:.0f} MB), more than the 126 MB L2",
+                   "timing": "K steps captured as CUDA graphs of the C-ABI calls and replayed; events around "
+                             "each step's prefill call inside the graphs"},
+        "ms_per_step_without_event_nodes": round(ms_plain, 4),
+        "prefill_tokens_per_s": round(_job_rate(P, n, pre_ms), 1),
+        "roofline": roof,
+        "e2e": {"value": round(_job_rate(P, n, e2e_ms), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h_x.numel() * 2, "d2h_bytes_per_step": h_o.numel() * 2},
+        # q_proj 2, append 1, prefill 2 (expansion, attention)
+        "gpu_launches": 5 * args.steps,
+        "clocks": res_t["clk"],
+    }
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline_prefill(P, args.cpu_budget)
     return res
 
 
@@ -620,10 +794,73 @@ def cpu_baseline(lens, qc, workload: str, budget_s: float = 15.0):
             "wall_s": round(time.perf_counter() - t_start, 1)}
 
 
+def _oracle_prefill(Wn, h_bf16):
+    """The oracle's prefill of a prompt (cache rows and query parts from h,
+    expanded K/V, causal attention); the output projection is left out, as
+    in the GPU prefill call."""
+    import oracle as O
+    d = synth.V2
+    return O.prefill_expanded(O.f64(h_bf16), Wn, n_h=d.n_h, base=d.rope_base, with_u=False)
+
+
+def _prefill_sample(P: int, budget_s: float):
+    """The oracle's prefill of the largest power-of-two prompt prefix (64
+    tokens up to P) that fits budget_s: prefixes double while four times the
+    last one's time (an upper bound on the doubled prefix's, whose work grows
+    at most with the square) stays within the budget.  Returns the weights,
+    the prompt, the prefix length and its time."""
+    Wn, _ = _oracle_inputs(1)
+    h = synth.hidden(P, synth.V2, SEED, name="h_prompt", device="cpu")
+    n = min(64, P)
+    t0 = time.perf_counter()
+    _oracle_prefill(Wn, h[:n])
+    el = time.perf_counter() - t0
+    while 2 * n <= P and 4 * el <= budget_s:
+        n *= 2
+        t0 = time.perf_counter()
+        _oracle_prefill(Wn, h[:n])
+        el = time.perf_counter() - t0
+    return Wn, h, n, el
+
+
+def cpu_baseline_prefill(P: int, budget_s: float = 15.0):
+    t_start = time.perf_counter()
+    _, _, n, el = _prefill_sample(P, budget_s)
+    return {"value": round(n / el, 4), "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"the first {n} of the {P} prompt tokens through the oracle's prefill (expanded K/V, fp64 "
+                      f"numpy; attention cost grows with the prefix's square, so this rate is above the full "
+                      f"prompt's), {el:.1f} s of oracle time",
+            "wall_s": round(time.perf_counter() - t_start, 1)}
+
+
+def run_reference_prefill(args):
+    P = args.seq_len if args.seq_len is not None else WORKLOADS[args.workload]["P"]
+    Wn, h, n, _ = _prefill_sample(P, max(1.0, args.cpu_budget / max(1, args.steps)))
+    total = 0.0
+    for s in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        _oracle_prefill(Wn, h[:n])
+        if s >= args.warmup:
+            total += time.perf_counter() - t0
+    v = n * args.steps / total
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "tokens/s", "n_gpus": _dist()[0],
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"MLA prefill, one prompt of P={P} tokens", "batch": 1, "tokens_per_step": P,
+                   "seq_len": P},
+        "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+                         "sample": f"each step = the oracle's prefill of the first {n} of the {P} prompt tokens"},
+        "e2e": {"value": round(v, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args):
     ws, rank = _dist()
     if rank != 0:
         return None
+    if WORKLOADS[args.workload]["kind"] == "prefill":
+        return run_reference_prefill(args)
     lens, qc, _, desc = workload_shape(args.workload, args.batch, args.seq_len)
     toks = _token_list(lens, qc)
     B = len(toks)
@@ -679,6 +916,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         res = run_reference(args)
+    elif WORKLOADS[args.workload]["kind"] == "prefill":
+        res = run_prefill(args)
     else:
         res = run_ours(args)
     if res is not None:

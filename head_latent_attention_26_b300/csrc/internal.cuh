@@ -20,17 +20,17 @@ namespace mla {
 // so a handle encodes each one once and reuses it on later calls.
 struct MapKey {
   const void* base;
-  long long cols, rows;
+  long long cols, rows, ld;
   int box_cols, box_rows, swizzle, dtype;
   bool operator==(const MapKey& o) const {
-    return base == o.base && cols == o.cols && rows == o.rows && box_cols == o.box_cols &&
+    return base == o.base && cols == o.cols && rows == o.rows && ld == o.ld && box_cols == o.box_cols &&
            box_rows == o.box_rows && swizzle == o.swizzle && dtype == o.dtype;
   }
 };
 struct MapKeyHash {
   size_t operator()(const MapKey& k) const {
     size_t h = std::hash<const void*>()(k.base);
-    for (long long v : {k.cols, k.rows, static_cast<long long>(k.box_cols), static_cast<long long>(k.box_rows),
+    for (long long v : {k.cols, k.rows, k.ld, static_cast<long long>(k.box_cols), static_cast<long long>(k.box_rows),
                         static_cast<long long>(k.swizzle), static_cast<long long>(k.dtype)})
       h = h * 1000003u ^ std::hash<long long>()(v);
     return h;
@@ -172,11 +172,12 @@ cudaError_t launch_decode_tc(const mla_handle* h, const void* q_lat, const void*
 // cuTensorMapEncodeTiled from the driver (looked up once); null if unavailable.
 PFN_cuTensorMapEncodeTiled_v12000 tma_encoder();
 // A 2-D tiled tensor map of a row-major [rows, cols] tensor with boxes of
-// box_cols x box_rows, 16-bit (bf16) or 8-bit (u8) elements, encoded once per
-// handle and key and copied out of the handle's cache afterwards.
+// box_cols x box_rows, 16-bit (bf16) or 8-bit (u8) elements, rows `ld`
+// elements apart (0: cols), encoded once per handle and key and copied out of
+// the handle's cache afterwards.
 bool tensor_map_2d(const mla_handle* h, CUtensorMap* out, const void* base, long long cols, long long rows,
                    int box_cols, int box_rows, CUtensorMapSwizzle sw,
-                   CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+                   CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, long long ld = 0);
 // Sets a kernel's dynamic shared-memory size (and, when asked, the
 // non-portable cluster-size opt-in) the first time this handle launches it.
 cudaError_t kernel_attrs_once(const mla_handle* h, const void* fn, int smem_bytes, bool nonportable_cluster);
@@ -185,10 +186,15 @@ cudaError_t decode_noalloc_scratch_address(void** ptr);
 // tcgen05 projections (bf16, d_h = 128, widths multiples of 64)
 cudaError_t launch_linear_tc(const mla_handle* h, const void* X, int x_cols, const void* W, int in, int out,
                              int groups, int x_group_cols, void* Y, long long ldy, int n_tok, cudaStream_t s);
-// Two products of the same tokens in one launch: Y1 = X W1^T, Y2 = X W2^T.
+// Two products of the same tokens in one launch: Y1 = X W1^T, Y2 = X W2^T
+// (token rows of X are x_ld elements apart, 0: in; bit 0 / bit 1 of f16_mask
+// write Y1 / Y2 as fp16 instead of bf16).
 cudaError_t launch_linear2_tc(const mla_handle* h, const void* X, int in, const void* W1, int out1, void* Y1,
                               long long ldy1, const void* W2, int out2, void* Y2, long long ldy2, int n_tok,
-                              cudaStream_t s);
+                              cudaStream_t s, long long x_ld = 0, int f16_mask = 0);
+// Prefill attention over expanded keys and values (tcgen05): see mla_prefill.
+cudaError_t launch_prefill_attn_tc(const mla_handle* h, const void* rows, const void* q_c, const void* q_r, int P,
+                                   const void* k_c, const void* v, void* o, float* lse, cudaStream_t s);
 cudaError_t launch_cache_append_tc(const mla_handle* h, const void* x, const void* w_dkr, const int* seq_idx,
                                    const int* pos, int n_new, const int* block_table, int max_blocks, int batch,
                                    void* pool, int n_pool_blocks, cudaStream_t s);

@@ -48,9 +48,10 @@ bool proj_tc_dims(const mla_dims* d) {
 namespace mla {
 
 bool tensor_map_2d(const mla_handle* h, CUtensorMap* out, const void* base, long long cols, long long rows,
-                   int box_cols, int box_rows, CUtensorMapSwizzle sw, CUtensorMapDataType dt) {
+                   int box_cols, int box_rows, CUtensorMapSwizzle sw, CUtensorMapDataType dt, long long ld) {
   const int eb = dt == CU_TENSOR_MAP_DATA_TYPE_UINT8 ? 1 : 2;
-  const MapKey key{base, cols, rows, box_cols, box_rows, static_cast<int>(sw), static_cast<int>(dt)};
+  if (ld <= 0) ld = cols;
+  const MapKey key{base, cols, rows, ld, box_cols, box_rows, static_cast<int>(sw), static_cast<int>(dt)};
   std::lock_guard<std::mutex> lock(h->mu);
   auto it = h->maps.find(key);
   if (it != h->maps.end()) {
@@ -60,7 +61,7 @@ bool tensor_map_2d(const mla_handle* h, CUtensorMap* out, const void* base, long
   auto enc = tma_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * eb};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * eb};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[2] = {1, 1};
   CUtensorMap m;
@@ -237,6 +238,36 @@ mla_status mla_cache_append_q8(mla_handle* h, const void* x, const void* w_dkr, 
                                                n_pool_blocks, ws, stream));
   MLA_TRY_CUDA(mla::launch_quantize_scatter_q8(h, ws, seq_idx, pos, n_new, block_table, max_blocks, batch, pool_q8,
                                                n_pool_blocks, stream));
+  return MLA_OK;
+}
+
+// ---------------------------------------------------------------- prefill
+size_t mla_prefill_workspace_bytes(const mla_handle* h, int P) {
+  if (!h || P < 0) return 0;
+  const size_t one = static_cast<size_t>(P) * h->dims.n_h * h->dims.d_h * 2;  // K^C or V, bf16
+  return 2 * ((one + 255) & ~static_cast<size_t>(255));
+}
+
+mla_status mla_prefill(mla_handle* h, const void* rows, const void* q_c, const void* q_r, int P, const void* w_uk,
+                       const void* w_uv, void* ws, size_t ws_bytes, void* o, float* lse, cudaStream_t stream) {
+  if (!h || P < 0) return MLA_ERR_INVALID_ARG;
+  if (!h->tensor_path || !h->proj_tc) return MLA_ERR_UNSUPPORTED;
+  if (P == 0) return MLA_OK;
+  if (P > h->max_pos) return MLA_ERR_INVALID_ARG;
+  for (const void* p : {rows, q_c, q_r, w_uk, w_uv, static_cast<const void*>(o)})
+    if (!p || !aligned16(p)) return MLA_ERR_INVALID_ARG;
+  if (!lse || !aligned4(lse)) return MLA_ERR_INVALID_ARG;
+  if (!ws || !aligned16(ws) || ws_bytes < mla_prefill_workspace_bytes(h, P)) return MLA_ERR_WORKSPACE;
+  const mla_dims& d = h->dims;
+  const int cols = d.n_h * d.d_h;
+  uint8_t* k_c = static_cast<uint8_t*>(ws);
+  uint8_t* v = k_c + mla_prefill_workspace_bytes(h, P) / 2;
+  // K^C = C W^UK^T and V = C W^UV^T for every head at once, in fp16 (the
+  // attention multiplies fp16 operands); C = the first d_c columns of each
+  // cache row
+  MLA_TRY_CUDA(mla::launch_linear2_tc(h, rows, d.d_c, w_uk, cols, k_c, cols, w_uv, cols, v, cols, P, stream,
+                                      d.d_c + d.d_hr, 3));
+  MLA_TRY_CUDA(mla::launch_prefill_attn_tc(h, rows, q_c, q_r, P, k_c, v, o, lse, stream));
   return MLA_OK;
 }
 

@@ -35,6 +35,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -72,6 +73,7 @@ struct ProjParams {
   int seg1_tiles, out2;
   __nv_bfloat16* y2;
   long long ldy2;
+  int y_f16, y2_f16;  // linear mode: write y / y2 as fp16 instead of bf16
   // append
   const int* seq_idx;
   const int* pos;
@@ -111,6 +113,15 @@ __device__ __forceinline__ bool proj_wait(uint64_t* bar, uint32_t parity, const 
 
 __device__ __forceinline__ void store_pair(__nv_bfloat16* dst, float a, float b) {
   *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(a, b);
+}
+// the same pair as bf16 or, when f16, as fp16 (one rounding either way)
+__device__ __forceinline__ void store_pair_as(__nv_bfloat16* dst, float a, float b, int f16) {
+  if (f16) {
+    const __half2 v = __floats2half2_rn(a, b);
+    *reinterpret_cast<__half2*>(dst) = v;
+  } else {
+    store_pair(dst, a, b);
+  }
 }
 
 // One CTA computes MT output tiles of 128 weight rows (one TMEM accumulator of
@@ -321,8 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
           const float2 a = pr[e];
           if (MODE == kModeLinear) {
             const int o = o_tile * kBM + row;
-            if (!seg2 && o < p.out) store_pair(p.y + static_cast<size_t>(n) * p.ldy + o, a.x, a.y);
-            if (seg2 && o < p.out2) store_pair(p.y2 + static_cast<size_t>(n) * p.ldy2 + o, a.x, a.y);
+            if (!seg2 && o < p.out) store_pair_as(p.y + static_cast<size_t>(n) * p.ldy + o, a.x, a.y, p.y_f16);
+            if (seg2 && o < p.out2) store_pair_as(p.y2 + static_cast<size_t>(n) * p.ldy2 + o, a.x, a.y, p.y2_f16);
           } else if (MODE == kModeAppend) {
             const int o = o_tile * kBM + row;
             const int slot = ss->slot[c0 + col];
@@ -510,10 +521,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tma_encoder() {
   return fn;
 }
 
-// bf16 [rows, cols] with 128B-swizzled boxes, through the handle's map cache
+// bf16 [rows, cols] (rows ld elements apart; 0: cols) with 128B-swizzled
+// boxes, through the handle's map cache
 bool encode_bf16_2d(const mla_handle* h, CUtensorMap* m, const void* base, long long cols, long long rows,
-                    int box_cols, int box_rows) {
-  return tensor_map_2d(h, m, base, cols, rows, box_cols, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+                    int box_cols, int box_rows, long long ld = 0) {
+  return tensor_map_2d(h, m, base, cols, rows, box_cols, box_rows, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ld);
 }
 
 namespace {
@@ -556,11 +569,11 @@ cudaError_t launch_linear_tc(const mla_handle* h, const void* X, int x_cols, con
 
 cudaError_t launch_linear2_tc(const mla_handle* h, const void* X, int in, const void* W1, int out1, void* Y1,
                               long long ldy1, const void* W2, int out2, void* Y2, long long ldy2, int n_tok,
-                              cudaStream_t s) {
+                              cudaStream_t s, long long x_ld, int f16_mask) {
   ProjMaps maps;
   const int nt = token_tile(n_tok);
   if (!encode_bf16_2d(h, &maps.w, W1, in, out1, kBK, kBM) || !encode_bf16_2d(h, &maps.w2, W2, in, out2, kBK, kBM) ||
-      !encode_bf16_2d(h, &maps.x, X, in, n_tok, kBK, nt))
+      !encode_bf16_2d(h, &maps.x, X, in, n_tok, kBK, nt, x_ld))
     return cudaErrorInvalidValue;
   ProjParams p = base_params(h, n_tok);
   const int t1 = (out1 + kBM - 1) / kBM, t2 = (out2 + kBM - 1) / kBM;
@@ -571,6 +584,8 @@ cudaError_t launch_linear2_tc(const mla_handle* h, const void* X, int in, const 
   p.ldy = ldy1;
   p.y2 = static_cast<__nv_bfloat16*>(Y2);
   p.ldy2 = ldy2;
+  p.y_f16 = f16_mask & 1;
+  p.y2_f16 = (f16_mask >> 1) & 1;
   p.seg1_tiles = t1;
   return launch_proj<kModeLinear, 1>(h, maps, p, pick_split(h, t1 + t2, n_tok, p.k_blocks), t1 + t2, s);
 }

@@ -66,6 +66,8 @@ _SIGS = {
     "mla_decode": (I, [P, P, P, I, P, I, P, P, I, I, I, P, SZ, P, P, P]),
     "mla_decode_noalloc": (I, [P, P, P, I, P, I, P, P, I, I, I, P, P, P]),
     "mla_decode_q8": (I, [P, P, P, I, P, I, P, P, I, I, I, P, SZ, P, P, P]),
+    "mla_prefill_workspace_bytes": (SZ, [P, I]),
+    "mla_prefill": (I, [P, P, P, P, I, P, P, P, SZ, P, P, P]),
     "mla_out_workspace_bytes": (SZ, [P, I]),
     "mla_out": (I, [P, P, P, P, I, P, P, SZ, P]),
     "mla_check_device_status": (I, [P, P]),
@@ -273,6 +275,19 @@ class MLA:
                                            block_table.shape[1], _ptr(seq_lens), _ptr(cu_q), seq_lens.shape[0], n,
                                            num_workers, _ptr(o_lat), _ptr(lse), P(_stream())), "mla_decode_noalloc")
         return o_lat, lse
+
+    def prefill(self, rows, q_c, q_r, W_uk, W_uv, o=None, lse=None):
+        """mla_prefill: causal attention of a P-token prompt over its expanded
+        keys and values.  rows [P, d_c + d_hr] (the prompt's cache rows in
+        position order), q_c [P, n_h, d_h], q_r [P, n_h, d_hr] (before RoPE).
+        Returns o [P, n_h, d_h] and lse [P, n_h]."""
+        d, n = self.dims, rows.shape[0]
+        o = torch.empty(n, d.n_h, d.d_h, dtype=self.dtype, device=rows.device) if o is None else o
+        lse = torch.empty(n, d.n_h, dtype=torch.float32, device=rows.device) if lse is None else lse
+        ws = self.workspace("prefill", self.lib.mla_prefill_workspace_bytes(self.h, n))
+        _check(self.lib.mla_prefill(self.h, _ptr(rows), _ptr(q_c), _ptr(q_r), n, _ptr(W_uk), _ptr(W_uv), _ptr(ws),
+                                    ws.numel(), _ptr(o), _ptr(lse), P(_stream())), "mla_prefill")
+        return o, lse
 
     def out(self, o_lat, W_uv, W_o, u=None):
         d, n = self.dims, o_lat.shape[0]

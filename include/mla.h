@@ -210,7 +210,8 @@ mla_status mla_decode(mla_handle* h, const void* q_lat, const void* pool, int n_
 /* ---- a3 + a4 over the quantised latent cache -------------------------------
  * The attention of mla_decode with the cache rows of mla_cache_append_q8
  * ([0h-n0] "量子化との組み合わせ"): row j stands for [code_j * scale_(j/32) ;
- * k^R], and each value is rounded once to bf16 on chip before the MMAs.  The
+ * k^R], and each value is rounded once to fp16 on chip before the MMAs (which
+ * take fp16 operands for this path; the queries and P are rounded to fp16).  The
  * cache stream is 672 bytes per row instead of 1152.
  *   pool_q8 [n_pool_blocks, block, 672] bytes; every other argument, the
  *   workspace (mla_decode_workspace_bytes) and the outputs as in mla_decode.
@@ -250,6 +251,30 @@ mla_status mla_decode_noalloc(mla_handle* h, const void* q_lat, const void* pool
                               const int* block_table, int max_blocks, const int* seq_lens,
                               const int* cu_q, int batch, int n_tok, int num_workers, void* o_lat,
                               float* lse, cudaStream_t stream);
+
+/* ---- prefill over expanded keys and values ---------------------------------
+ * Causal attention of a whole prompt in the un-absorbed form the pages give
+ * for prefill: with many tokens at once the latent vectors are up-projected
+ * to full keys and values by a large matrix product ([perforder]
+ * "極限最適化の代償：MLA特有の学習負荷と独自Tritonカーネルという障壁"; the
+ * reference's "naive" branch, [kasblo] "「キャッシュを減らせた」と「その割合だけ
+ * 速い」は別の評価").  Per head i: K^C_i = C W^UK_i^T and V_i = C W^UV_i^T for
+ * the prompt's latent rows C; for query t and key j <= t ([qiita] "Attention
+ * 計算") s_tj = (q^C_t,i . K^C_j,i + RoPE_t(q^R_t,i) . k^R_j) / sqrt(d_h + d_hr),
+ * a softmax over j and o_t,i = sum_j a_tj V_j,i.  Positions are 0..P-1.
+ *   rows [P, d_c + d_hr]  the prompt's cache rows in position order, bf16, as
+ *                         mla_cache_append writes them (c^KV ; rotated k^R)
+ *   q_c [P, n_h, d_h], q_r [P, n_h, d_hr]  as mla_q_proj writes them (q^R
+ *                         before its rotation)
+ *   w_uk, w_uv [n_h*d_h, d_c]
+ *   ws: mla_prefill_workspace_bytes(h, P) bytes (K^C and V, fp16: the
+ *       attention multiplies fp16 operands with fp32 accumulation)
+ *   o [P, n_h, d_h] bf16 (output), lse [P, n_h] f32 natural log (output)
+ * P <= max_pos.  Tensor-path sizes only; others return MLA_ERR_UNSUPPORTED. */
+size_t mla_prefill_workspace_bytes(const mla_handle* h, int P);
+mla_status mla_prefill(mla_handle* h, const void* rows, const void* q_c, const void* q_r, int P,
+                       const void* w_uk, const void* w_uv, void* ws, size_t ws_bytes, void* o,
+                       float* lse, cudaStream_t stream);
 
 /* ---- a5: output ------------------------------------------------------------
  * o_i = W^UV_i o~_i ([kasblo] "V側は、小さな表現の加重和を先に求める") and

@@ -72,6 +72,7 @@ __all__ = [
     "decode_sequence",
     "decode_batch",
     "prefill_expanded",
+    "prefill_from_parts",
 ]
 
 
@@ -455,7 +456,7 @@ def decode_sequence(h_rows, h_query, t: int, W: dict, n_h: int, base: float = 10
     return res
 
 
-def prefill_expanded(h, W: dict, n_h: int, base: float = 10000.0):
+def prefill_expanded(h, W: dict, n_h: int, base: float = 10000.0, with_u: bool = True):
     """Causal attention for every token of a prompt at once, in the expanded form.
 
     [perforder] "極限最適化の代償：MLA特有の学習負荷と独自Tritonカーネルという障壁":
@@ -463,32 +464,50 @@ def prefill_expanded(h, W: dict, n_h: int, base: float = 10000.0):
     up-projection of the latent vector to full keys and values becomes a large
     matrix product; [kasblo] "「キャッシュを減らせた」と「その割合だけ速い」は別の評価"
     names the reference implementation's "naive" branch that keeps the
-    expanded K/V.  Row t of the prompt attends rows 0..t ([qiita] "Attention
-    計算").  All P queries of a head at once: S = (Q^C K^C^T + Q^R K^R^T) /
-    sqrt(d_h + d_h^R) over the P x P positions, entries with j > t set to -inf,
-    a row-wise softmax with its log-sum-exp, O = A V, then u = W^O [o].
+    expanded K/V.  The cache rows and query parts of the prompt come from h
+    (positions 0..P-1); the attention itself is prefill_from_parts.
 
-    h: [P, d].  Returns o [P, n_h, d_h], lse [P, n_h] and u [P, d].
+    h: [P, d].  Returns o [P, n_h, d_h], lse [P, n_h] and u [P, d] (None when
+    with_u is False: the output projection is then skipped, the rest is the
+    same arithmetic).
     """
     h = f64(h)
     P = h.shape[0]
     pos = np.arange(P)
     c, k_r = kv_latent(h, W["W_dkv"], W["W_kr"], pos, base)
     _, q_c, q_r_raw = query_parts(h, W["W_dq"], W["W_uq"], W["W_qr"], n_h)
-    q_r = rope(q_r_raw, pos[:, None], base)
+    o, lse = prefill_from_parts(c, k_r, q_c, q_r_raw, W["W_uk"], W["W_uv"], base)
+    u = np.stack([output_projection(o[t], W["W_o"]) for t in range(P)]) if with_u else None
+    return o, lse, u
+
+
+def prefill_from_parts(c, k_r, q_c, q_r_raw, W_uk, W_uv, base: float = 10000.0):
+    """The prompt's causal attention from its cache rows and query parts.
+
+    c [P, d_c] and k_r [P, d_hR] (already rotated) are the prompt's cache rows
+    in position order, q_c [P, n_h, d_h] and q_r_raw [P, n_h, d_hR] (before
+    rotation) its query parts.  Row t of the prompt attends rows 0..t
+    ([qiita] "Attention 計算").  All P queries of a head at once: K/V expanded
+    per head, S = (Q^C K^C^T + Q^R K^R^T) / sqrt(d_h + d_h^R) over the P x P
+    positions, entries with j > t set to -inf, a row-wise softmax with its
+    log-sum-exp, O = A V.  Returns o [P, n_h, d_h] and lse [P, n_h].
+    """
+    c, k_r, q_c = f64(c), f64(k_r), f64(q_c)
+    P, n_h = q_c.shape[0], q_c.shape[1]
+    pos = np.arange(P)
+    q_r = rope(f64(q_r_raw), pos[:, None], base)
     d_h, d_hr = q_c.shape[2], q_r.shape[2]
     inv = 1.0 / math.sqrt(d_h + d_hr)
     later = np.triu(np.ones((P, P), dtype=bool), 1)  # key j after query t
     o = np.empty((P, n_h, d_h))
     lse = np.empty((P, n_h))
     for i in range(n_h):
-        k_c, v = expand_kv(c, W["W_uk"], W["W_uv"], i, d_h)
+        k_c, v = expand_kv(c, W_uk, W_uv, i, d_h)
         s = (q_c[:, i] @ k_c.T + q_r[:, i] @ k_r.T) * inv
         s[later] = -np.inf
         a, lse[:, i] = softmax_lse(s)
         o[:, i] = a @ v
-    u = np.stack([output_projection(o[t], W["W_o"]) for t in range(P)])
-    return o, lse, u
+    return o, lse
 
 
 def decode_batch(q_lat, pool_rows, block_table, seq_lens, cu_q, block: int, d_c: int, d_h: int,

@@ -90,6 +90,25 @@ def _folded_weight_head_shift(orig):
     return bad
 
 
+def _prefill_parts_mask_includes_next_key(orig):
+    # the same planted mask error, in the attention from the prompt's parts
+    def bad(c, k_r, q_c, q_r_raw, W_uk, W_uv, base=10000.0):
+        c, k_r, q_c = M.f64(c), M.f64(k_r), M.f64(q_c)
+        P, n_h = q_c.shape[0], q_c.shape[1]
+        q_r = M.rope(M.f64(q_r_raw), np.arange(P)[:, None], base)
+        d_h, d_hr = q_c.shape[2], q_r.shape[2]
+        later = np.triu(np.ones((P, P), dtype=bool), 2)
+        o, lse = np.empty((P, n_h, d_h)), np.empty((P, n_h))
+        for i in range(n_h):
+            k_c, v = M.expand_kv(c, W_uk, W_uv, i, d_h)
+            s = (q_c[:, i] @ k_c.T + q_r[:, i] @ k_r.T) / np.sqrt(d_h + d_hr)
+            s[later] = -np.inf
+            a, lse[:, i] = M.softmax_lse(s)
+            o[:, i] = a @ v
+        return o, lse
+    return bad
+
+
 def _prefill_mask_includes_next_key(orig):
     # the causal mask lets row t see row t+1
     def bad(h, W, n_h, base=10000.0):
@@ -123,6 +142,7 @@ MUTATIONS = [
     ("quantize_q8_blocks", _q8_round_half_even),
     ("absorbed_query_weight", _folded_weight_head_shift),
     ("prefill_expanded", _prefill_mask_includes_next_key),
+    ("prefill_from_parts", _prefill_parts_mask_includes_next_key),
 ]
 
 
