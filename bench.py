@@ -13,8 +13,9 @@ permutation of the pool):
   prefill_p4096  a P=4096-token prompt: query projection, cache rows, and
                causal attention over the expanded keys and values
 
-One step = the whole path for the step's new tokens: query projection, cache
-append, W^UK absorption, latent attention (+ split combine), W^UV / W^O output.
+One step = the whole path for the step's new tokens: query projection with
+the cache append (mla_q_proj_append), W^UK absorption, latent attention
+(+ split combine), W^UV / W^O output.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME]
@@ -472,11 +473,12 @@ def run_ours(args):
         if pairs is not None:
             ea = torch.cuda.Event(enable_timing=True, external=True)
             ea.record()
-        m.q_proj(x, W["W_dq"], W["W_uq"], W["W_qr"], bufs["q_c"], bufs["q_r"])
         if q8:
+            m.q_proj(x, W["W_dq"], W["W_uq"], W["W_qr"], bufs["q_c"], bufs["q_r"])
             m.cache_append_q8(x, W_dkr, inp["seq_idx"], inp["pos"], table, pool)
         else:
-            m.cache_append(x, W_dkr, inp["seq_idx"], inp["pos"], table, pool)
+            m.q_proj_append(x, W["W_dq"], W["W_uq"], W["W_qr"], W_dkr, inp["seq_idx"], inp["pos"], table, pool,
+                            bufs["q_c"], bufs["q_r"])
         if pairs is not None:
             eb = torch.cuda.Event(enable_timing=True, external=True)
             eb.record()
@@ -515,10 +517,11 @@ def run_ours(args):
     # decode + combine), each between event nodes on the step's stream
     app_ms = sum(ea.elapsed_time(eb) for ea, eb, _, _ in pairs) / len(pairs)
     dec_ms = sum(e0.elapsed_time(e1) for _, _, e0, e1 in pairs) / len(pairs)
-    # kernels per step: q_proj 2 (W^DQ; W^UQ with W^QR), append 1 (quantised
-    # cache: 2, the rows then their codes), absorb 1, decode 3 (plan,
-    # attention, combine), out 2 (W^UV, W^O)
-    n_launch = 10 if q8 else 9
+    # kernels per step: query projection and append 2 (W^DQ with the cache
+    # rows; W^UQ with W^QR) -- the quantised cache: q_proj 2 and append 2
+    # (the rows, then their codes) --, absorb 1, decode 3 (plan, attention,
+    # combine), out 2 (W^UV, W^O)
+    n_launch = 10 if q8 else 8
 
     ms, ms_plain, dec_ms, app_ms, e2e_ms = _max_over_ranks([ms, ms_plain, dec_ms, app_ms, e2e_ms], ws)
     if rank != 0:

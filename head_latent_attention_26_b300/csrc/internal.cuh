@@ -195,6 +195,11 @@ cudaError_t launch_linear2_tc(const mla_handle* h, const void* X, int in, const 
 // Prefill attention over expanded keys and values (tcgen05): see mla_prefill.
 cudaError_t launch_prefill_attn_tc(const mla_handle* h, const void* rows, const void* q_c, const void* q_r, int P,
                                    const void* k_c, const void* v, void* o, float* lse, cudaStream_t s);
+// W^DQ and the cache-row product of the same tokens in one launch.
+cudaError_t launch_q_down_append_tc(const mla_handle* h, const void* x, const void* w_dq, void* c_q,
+                                   const void* w_dkr, const int* seq_idx, const int* pos, int n_new,
+                                   const int* block_table, int max_blocks, int batch, void* pool, int n_pool_blocks,
+                                   cudaStream_t s);
 cudaError_t launch_cache_append_tc(const mla_handle* h, const void* x, const void* w_dkr, const int* seq_idx,
                                    const int* pos, int n_new, const int* block_table, int max_blocks, int batch,
                                    void* pool, int n_pool_blocks, cudaStream_t s);

@@ -215,6 +215,35 @@ mla_status mla_cache_append(mla_handle* h, const void* x, const void* w_dkr, con
   return MLA_OK;
 }
 
+// ---------------------------------------------------------------- a0 + a1 in one call
+mla_status mla_q_proj_append(mla_handle* h, const void* x, const void* w_dq, const void* w_uq, const void* w_qr,
+                             const void* w_dkr, const int* seq_idx, const int* pos, int n_tok,
+                             const int* block_table, int max_blocks, int batch, void* pool, int n_pool_blocks,
+                             void* q_c, void* q_r, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!h || n_tok < 0) return MLA_ERR_INVALID_ARG;
+  if (n_tok == 0) return MLA_OK;
+  for (const void* p : {x, w_dq, w_uq, w_qr, w_dkr, static_cast<const void*>(pool), static_cast<const void*>(q_c),
+                        static_cast<const void*>(q_r)})
+    if (!p || !aligned16(p)) return MLA_ERR_INVALID_ARG;
+  if (!seq_idx || !pos || !block_table || !aligned4(seq_idx) || !aligned4(pos) || !aligned4(block_table))
+    return MLA_ERR_INVALID_ARG;
+  if (max_blocks < 1 || batch < 1 || n_pool_blocks < 1) return MLA_ERR_INVALID_ARG;
+  if (!ws || !aligned16(ws) || ws_bytes < mla_q_proj_workspace_bytes(h, n_tok)) return MLA_ERR_WORKSPACE;
+  if (!h->proj_tc) {
+    // the generic kernels: the two calls one after the other
+    const mla_status st = mla_q_proj(h, x, w_dq, w_uq, w_qr, n_tok, q_c, q_r, ws, ws_bytes, stream);
+    if (st != MLA_OK) return st;
+    return mla_cache_append(h, x, w_dkr, seq_idx, pos, n_tok, block_table, max_blocks, batch, pool, n_pool_blocks,
+                            stream);
+  }
+  const mla_dims& d = h->dims;
+  MLA_TRY_CUDA(mla::launch_q_down_append_tc(h, x, w_dq, ws, w_dkr, seq_idx, pos, n_tok, block_table, max_blocks,
+                                            batch, pool, n_pool_blocks, stream));
+  MLA_TRY_CUDA(mla::launch_linear2_tc(h, ws, d.d_cq, w_uq, d.n_h * d.d_h, q_c, d.n_h * d.d_h, w_qr,
+                                      d.n_h * d.d_hr, q_r, d.n_h * d.d_hr, n_tok, stream));
+  return MLA_OK;
+}
+
 // ---------------------------------------------------------------- a1, quantised cache
 size_t mla_cache_append_q8_workspace_bytes(const mla_handle* h, int n_new) {
   if (!h || n_new < 0) return 0;

@@ -53,7 +53,7 @@ constexpr int kThreads = 128;
 constexpr int kMaxSplit = 16;                  // cluster size (above 8 needs the non-portable opt-in)
 constexpr int kMaxDevices = 16;                // devices whose resident-cluster counts are cached
 
-enum : int { kModeLinear = 0, kModeAppend = 1, kModeAbsorb = 2, kModeQFolded = 3 };
+enum : int { kModeLinear = 0, kModeAppend = 1, kModeAbsorb = 2, kModeQFolded = 3, kModeLinearAppend = 4 };
 
 struct ProjMaps {
   CUtensorMap w;   // weights
@@ -143,7 +143,11 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
   const int n0 = blockIdx.z * NT;
   // first output tile of this CTA; in linear mode tiles past seg1_tiles are
   // tiles of the second product
-  const bool seg2 = (MODE == kModeLinear || MODE == kModeQFolded) && static_cast<int>(blockIdx.y) * MT >= p.seg1_tiles;
+  const bool seg2 = (MODE == kModeLinear || MODE == kModeQFolded || MODE == kModeLinearAppend) &&
+                    static_cast<int>(blockIdx.y) * MT >= p.seg1_tiles;
+  // tiles that write cache rows: every tile of the append mode, the second
+  // product's tiles of the linear + append mode
+  const bool appends = MODE == kModeAppend || (MODE == kModeLinearAppend && seg2);
   const int tile0 = static_cast<int>(blockIdx.y) * MT - (seg2 ? p.seg1_tiles : 0);
   const CUtensorMap* wmap = seg2 ? &maps.w2 : &maps.w;
   const int group = tile0 / p.tiles_per_group;  // all MT tiles share it (MT divides tiles_per_group)
@@ -247,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
       }
       mma_commit_elect(&ss->done);  // arrives once every MMA above has finished
     }
-  } else if (MODE == kModeAppend) {
+  } else if (appends) {
     // ---------------------------------------------------------------- destination rows
     pdl_wait();
     for (int j = threadIdx.x - 64; j < NT; j += 64) {
@@ -330,14 +334,14 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
         for (int e = 0; e < 2; ++e) {
           const int row = row0 + 2 * e;
           const float2 a = pr[e];
-          if (MODE == kModeLinear) {
+          if (MODE == kModeLinear || (MODE == kModeLinearAppend && !seg2)) {
             const int o = o_tile * kBM + row;
             if (!seg2 && o < p.out) store_pair_as(p.y + static_cast<size_t>(n) * p.ldy + o, a.x, a.y, p.y_f16);
             if (seg2 && o < p.out2) store_pair_as(p.y2 + static_cast<size_t>(n) * p.ldy2 + o, a.x, a.y, p.y2_f16);
-          } else if (MODE == kModeAppend) {
+          } else if (appends) {
             const int o = o_tile * kBM + row;
             const int slot = ss->slot[c0 + col];
-            if (o >= p.out || slot < 0) continue;
+            if (o >= (MODE == kModeLinearAppend ? p.out2 : p.out) || slot < 0) continue;
             __nv_bfloat16* dst = p.pool + static_cast<size_t>(slot) * p.width + o;
             if (o < p.d_c) {
               store_pair(dst, a.x, a.y);
@@ -632,6 +636,38 @@ cudaError_t launch_cache_append_tc(const mla_handle* h, const void* x, const voi
   maps.w2 = maps.w;
   p.seg1_tiles = 1 << 30;
   return launch_proj<kModeAppend, 1>(h, maps, p, pick_split(h, o_tiles, n_new, p.k_blocks), o_tiles, s);
+}
+
+// c^Q = W^DQ x (into c_q, [n_tok, d_cq]) and the cache rows of the same tokens
+// (mla_cache_append's product and epilogue) in one launch: both products
+// read the same token tiles.
+cudaError_t launch_q_down_append_tc(const mla_handle* h, const void* x, const void* w_dq, void* c_q,
+                                   const void* w_dkr, const int* seq_idx, const int* pos, int n_new,
+                                   const int* block_table, int max_blocks, int batch, void* pool, int n_pool_blocks,
+                                   cudaStream_t s) {
+  const mla_dims& d = h->dims;
+  const int width = d.d_c + d.d_hr;
+  ProjMaps maps;
+  if (!encode_bf16_2d(h, &maps.w, w_dq, d.d_model, d.d_cq, kBK, kBM) ||
+      !encode_bf16_2d(h, &maps.w2, w_dkr, d.d_model, width, kBK, kBM) ||
+      !encode_bf16_2d(h, &maps.x, x, d.d_model, n_new, kBK, token_tile(n_new)))
+    return cudaErrorInvalidValue;
+  ProjParams p = base_params(h, n_new);
+  const int t1 = (d.d_cq + kBM - 1) / kBM, t2 = (width + kBM - 1) / kBM;
+  p.out = d.d_cq;
+  p.y = static_cast<__nv_bfloat16*>(c_q);
+  p.ldy = d.d_cq;
+  p.out2 = width;
+  p.seg1_tiles = t1;
+  p.k_blocks = (d.d_model + kBK - 1) / kBK;
+  p.seq_idx = seq_idx;
+  p.pos = pos;
+  p.block_table = block_table;
+  p.max_blocks = max_blocks;
+  p.batch = batch;
+  p.n_pool_blocks = n_pool_blocks;
+  p.pool = static_cast<__nv_bfloat16*>(pool);
+  return launch_proj<kModeLinearAppend, 1>(h, maps, p, pick_split(h, t1 + t2, n_new, p.k_blocks), t1 + t2, s);
 }
 
 // The cache rows of the new tokens, [n_new, d_c + d_hr] bf16 in token order

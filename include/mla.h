@@ -124,6 +124,19 @@ mla_status mla_cache_append(mla_handle* h, const void* x, const void* w_dkr, con
                             const int* pos, int n_new, const int* block_table, int max_blocks,
                             int batch, void* pool, int n_pool_blocks, cudaStream_t stream);
 
+/* ---- a0 + a1 in one call ---------------------------------------------------
+ * mla_q_proj and mla_cache_append for the same new tokens (x is their input
+ * h, n_tok of them), with the two products that read x -- c^Q = W^DQ x and
+ * the cache rows [W^DKV x ; RoPE_pos(W^KR x)] -- issued as one launch.  The
+ * arguments are those of the two calls (ws: mla_q_proj_workspace_bytes(h,
+ * n_tok) bytes); the results are theirs up to the order of the fp32 sums.
+ * Sizes outside the tensor path run the two calls one after the other. */
+mla_status mla_q_proj_append(mla_handle* h, const void* x, const void* w_dq, const void* w_uq,
+                             const void* w_qr, const void* w_dkr, const int* seq_idx, const int* pos,
+                             int n_tok, const int* block_table, int max_blocks, int batch, void* pool,
+                             int n_pool_blocks, void* q_c, void* q_r, void* ws, size_t ws_bytes,
+                             cudaStream_t stream);
+
 /* ---- a1 with the quantised latent cache -------------------------------------
  * [0h-n0] "量子化との組み合わせ": c^KV can further be stored with KV-cache
  * quantisation of the Q8_0 kind.  Each cached row becomes 672 bytes:

@@ -243,6 +243,47 @@ def test_v2_layer_end_to_end(v2):
     assert all(e < OUT_TOL for e in errs.values()) and e_l < LSE_TOL, (errs, e_l)
 
 
+@pytest.mark.parametrize("n_new", [1, 64, 300])
+def test_q_proj_append_matches_the_two_calls(v2, n_new):
+    """mla_q_proj_append (W^DQ and the cache-row product in one launch) against
+    mla_q_proj + mla_cache_append on the same tokens: the same pool rows
+    written (every other row keeps its sentinel, bit for bit), the rows and
+    the query parts equal up to the order of the fp32 sums, and both against
+    the oracle's cache rows and query parts."""
+    d = V2
+    seed = 1400 + n_new
+    W = synth.weights(d, seed, device="cuda")
+    x = synth.hidden(n_new, d, seed, device="cuda")
+    lens = [n_new + 37]
+    table, n_blocks, _, _, _ = batch_meta(lens, [n_new], d.block, seed, spare_blocks=2)
+    seq_idx = torch.zeros(n_new, dtype=torch.int32, device="cuda")
+    pos = torch.arange(37, 37 + n_new, dtype=torch.int32, device="cuda")
+    sentinel = torch.full((n_blocks, d.block, d.width), 0x3F3F, dtype=torch.int16, device="cuda")
+    pool_a = sentinel.clone().view(torch.bfloat16)
+    pool_b = sentinel.clone().view(torch.bfloat16)
+    q_c_a, q_r_a = v2.q_proj_append(x, W["W_dq"], W["W_uq"], W["W_qr"], _w_dkr(W), seq_idx, pos, table, pool_a)
+    q_c_b, q_r_b = v2.q_proj(x, W["W_dq"], W["W_uq"], W["W_qr"])
+    v2.cache_append(x, _w_dkr(W), seq_idx, pos, table, pool_b)
+    v2.check()
+    written_a = pool_a.view(torch.int16) != 0x3F3F
+    written_b = pool_b.view(torch.int16) != 0x3F3F
+    assert torch.equal(written_a.any(-1), written_b.any(-1))
+    tab = table.cpu()
+    slots = [O.cache_slot(tab, 0, int(p_), d.block) for p_ in pos.tolist()]
+    rows_a = pool_a.view(-1, d.width)[slots]
+    rows_b = pool_b.view(-1, d.width)[slots]
+    assert int(written_a.view(-1, d.width).any(-1).sum()) == n_new
+    assert row_rel_err(to_np(rows_a), to_np(rows_b)) < 2 ** -7
+    assert row_rel_err(to_np(q_c_a), to_np(q_c_b)) < 2 ** -6 and row_rel_err(to_np(q_r_a), to_np(q_r_b)) < 2 ** -6
+    Wn = _np_weights(W)
+    c_ref, kr_ref = O.kv_latent(to_np(x), Wn["W_dkv"], Wn["W_kr"], pos.cpu().numpy(), d.rope_base)
+    _, qc_ref, qr_ref = O.query_parts(to_np(x), Wn["W_dq"], Wn["W_uq"], Wn["W_qr"], d.n_h)
+    e_rows = row_rel_err(to_np(rows_a), np.concatenate([c_ref, kr_ref], axis=1))
+    e_qc, e_qr = row_rel_err(to_np(q_c_a), qc_ref), row_rel_err(to_np(q_r_a), qr_ref)
+    record("q_proj_append: cache rows / q_c / q_r", max(e_rows, e_qc, e_qr))
+    assert e_rows < OUT_TOL and e_qc < OUT_TOL and e_qr < OUT_TOL, (e_rows, e_qc, e_qr)
+
+
 # ---------------------------------------------------------------------------
 # Full-size workloads, sampled outputs, in the launch configuration of the bench
 # ---------------------------------------------------------------------------
