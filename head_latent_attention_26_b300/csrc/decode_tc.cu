@@ -1019,7 +1019,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ seq_
 // Merge the pieces of every token whose keys were split across workers:
 // lse = ln sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s (the standard
 // identity for a softmax split over disjoint key ranges; not on the pages).
-// One CTA per (token, head); the pieces of a token are the workers g0..g1
+// Each CTA takes (token, head) pairs blockIdx.x, blockIdx.x + gridDim.x, ...
+// (at most eight CTAs per SM, so a call that split nothing costs one short
+// wave of early exits); the pieces of a token are the workers g0..g1
 // whose ranges meet its tiles.  Worker g wrote slot 2g when its range starts
 // inside the token, else 2g+1 (its range started in an earlier token).  The
 // pieces are spread over the CTA's eight warps (each lane holds 16 of the 512
@@ -1044,75 +1046,81 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(
   pdl_wait();
   // The next decode call's plan may overwrite the plan data, so the next
   // kernel may launch only once every CTA has read all of it: CTAs that stop
-  // here exit (an exit counts as the trigger); the others trigger after the
-  // checks below have consumed every value they read.
+  // here exit (an exit counts as the trigger); the others trigger once they
+  // have read the plan values of their last pair (the merge itself reads only
+  // the partials, which the next call rewrites only after this grid ends).
   if (__ldg(plan_flags) == 0) return;  // whole tokens per worker: nothing was split
-  const int n = blockIdx.x, h = blockIdx.y;
   const int total = __ldg(prefix + n_tok);
-  const int t0 = __ldg(prefix + n), t1 = __ldg(prefix + n + 1);
-  if (t1 <= t0) return;
-  const int g0 = worker_of(t0, workers, total), g1 = worker_of(t1 - 1, workers, total);
-  if (g0 == g1) return;  // whole token inside one worker: already final
-  __syncthreads();
-  if (threadIdx.x == 0) pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int npieces = g1 - g0 + 1;
-  // L = ln sum_s exp(lse_s), block-wide: max, then the sum of exponentials
-  float mx = -INFINITY;
-  for (int k = threadIdx.x; k < npieces; k += blockDim.x) {
-    const int slot = piece_slot(k, g0, t0, workers, total);
-    if (slot >= 0) mx = fmaxf(mx, __ldg(part_lse + static_cast<size_t>(slot) * kHeads + h));
-  }
-  mx = warp_max(mx);
-  if (lane == 0) s_red[warp] = mx;
-  __syncthreads();
-  mx = s_red[0];
+  for (int pair = blockIdx.x; pair < n_tok * kHeads; pair += gridDim.x) {
+    const int n = pair / kHeads, h = pair % kHeads;
+    const int t0 = __ldg(prefix + n), t1 = __ldg(prefix + n + 1);
+    if (pair + static_cast<int>(gridDim.x) >= n_tok * kHeads) {  // this CTA's last pair
+      __syncthreads();
+      if (threadIdx.x == 0) pdl_trigger();
+    }
+    if (t1 <= t0) continue;
+    const int g0 = worker_of(t0, workers, total), g1 = worker_of(t1 - 1, workers, total);
+    if (g0 == g1) continue;  // whole token inside one worker: already final
+    const int npieces = g1 - g0 + 1;
+    // L = ln sum_s exp(lse_s), block-wide: max, then the sum of exponentials
+    float mx = -INFINITY;
+    for (int k = threadIdx.x; k < npieces; k += blockDim.x) {
+      const int slot = piece_slot(k, g0, t0, workers, total);
+      if (slot >= 0) mx = fmaxf(mx, __ldg(part_lse + static_cast<size_t>(slot) * kHeads + h));
+    }
+    mx = warp_max(mx);
+    if (lane == 0) s_red[warp] = mx;
+    __syncthreads();
+    mx = s_red[0];
 #pragma unroll
-  for (int w = 1; w < kCombineWarps; ++w) mx = fmaxf(mx, s_red[w]);
-  __syncthreads();
-  float sum = 0.f;
-  for (int k = threadIdx.x; k < npieces; k += blockDim.x) {
-    const int slot = piece_slot(k, g0, t0, workers, total);
-    if (slot >= 0) sum += expf(__ldg(part_lse + static_cast<size_t>(slot) * kHeads + h) - mx);
-  }
-  sum = warp_sum(sum);
-  if (lane == 0) s_red[warp] = sum;
-  __syncthreads();
-  sum = 0.f;
+    for (int w = 1; w < kCombineWarps; ++w) mx = fmaxf(mx, s_red[w]);
+    __syncthreads();
+    float sum = 0.f;
+    for (int k = threadIdx.x; k < npieces; k += blockDim.x) {
+      const int slot = piece_slot(k, g0, t0, workers, total);
+      if (slot >= 0) sum += expf(__ldg(part_lse + static_cast<size_t>(slot) * kHeads + h) - mx);
+    }
+    sum = warp_sum(sum);
+    if (lane == 0) s_red[warp] = sum;
+    __syncthreads();
+    sum = 0.f;
 #pragma unroll
-  for (int w = 0; w < kCombineWarps; ++w) sum += s_red[w];
-  const float L = mx + logf(sum);
-  // o = sum_s exp(lse_s - L) o_s: warp w takes pieces w, w + 8, ...
-  float4 acc[4];
+    for (int w = 0; w < kCombineWarps; ++w) sum += s_red[w];
+    const float L = mx + logf(sum);
+    // o = sum_s exp(lse_s - L) o_s: warp w takes pieces w, w + 8, ...
+    float4 acc[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 2
-  for (int k = warp; k < npieces; k += kCombineWarps) {
-    const int slot = piece_slot(k, g0, t0, workers, total);
-    if (slot < 0) continue;
-    const float wk = expf(__ldg(part_lse + static_cast<size_t>(slot) * kHeads + h) - L);
-    const float4* src = reinterpret_cast<const float4*>(part_o + (static_cast<size_t>(slot) * kHeads + h) * kDc);
+    for (int k = warp; k < npieces; k += kCombineWarps) {
+      const int slot = piece_slot(k, g0, t0, workers, total);
+      if (slot < 0) continue;
+      const float wk = expf(__ldg(part_lse + static_cast<size_t>(slot) * kHeads + h) - L);
+      const float4* src = reinterpret_cast<const float4*>(part_o + (static_cast<size_t>(slot) * kHeads + h) * kDc);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float4 v = __ldg(src + lane + 32 * j);
-      acc[j].x += wk * v.x; acc[j].y += wk * v.y; acc[j].z += wk * v.z; acc[j].w += wk * v.w;
+      for (int j = 0; j < 4; ++j) {
+        const float4 v = __ldg(src + lane + 32 * j);
+        acc[j].x += wk * v.x; acc[j].y += wk * v.y; acc[j].z += wk * v.z; acc[j].w += wk * v.w;
+      }
     }
-  }
 #pragma unroll
-  for (int j = 0; j < 4; ++j) s_acc[warp][lane + 32 * j] = acc[j];
-  __syncthreads();
-  // thread i finishes the 4 columns of float4 slot i (i < 128) of the 512
-  if (threadIdx.x < kDc / 4) {
-    float4 o = s_acc[0][threadIdx.x];
+    for (int j = 0; j < 4; ++j) s_acc[warp][lane + 32 * j] = acc[j];
+    __syncthreads();
+    // thread i finishes the 4 columns of float4 slot i (i < 128) of the 512
+    if (threadIdx.x < kDc / 4) {
+      float4 o = s_acc[0][threadIdx.x];
 #pragma unroll
-    for (int w = 1; w < kCombineWarps; ++w) {
-      const float4 v = s_acc[w][threadIdx.x];
-      o.x += v.x; o.y += v.y; o.z += v.z; o.w += v.w;
+      for (int w = 1; w < kCombineWarps; ++w) {
+        const float4 v = s_acc[w][threadIdx.x];
+        o.x += v.x; o.y += v.y; o.z += v.z; o.w += v.w;
+      }
+      __nv_bfloat16* dst = o_lat + (static_cast<size_t>(n) * kHeads + h) * kDc + 4 * threadIdx.x;
+      *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
     }
-    __nv_bfloat16* dst = o_lat + (static_cast<size_t>(n) * kHeads + h) * kDc + 4 * threadIdx.x;
-    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
+    if (threadIdx.x == 0) lse[static_cast<size_t>(n) * kHeads + h] = L;
+    __syncthreads();  // s_red and s_acc are reused by the next pair
   }
-  if (threadIdx.x == 0) lse[static_cast<size_t>(n) * kHeads + h] = L;
 }
 
 bool encode_pool_maps(const mla_handle* h, Maps* maps, const void* pool, long long rows) {
@@ -1145,7 +1153,8 @@ cudaError_t launch_decode_kernels(const mla_handle* h, const Maps& maps, const P
   if (e != cudaSuccess) return e;
   e = launch_pdl(decode_tc_kernel<Q8>, dim3(2 * W), dim3(kThreads), kSmemBytes, s, 1, maps, prm);
   if (e != cudaSuccess) return e;
-  return launch_pdl(combine_kernel, dim3(n_tok, kHeads), dim3(32 * kCombineWarps), 0, s, 1, static_cast<const int*>(prm.prefix),
+  const int pairs = n_tok * kHeads, grid = pairs < 8 * h->num_sms ? pairs : 8 * h->num_sms;
+  return launch_pdl(combine_kernel, dim3(grid), dim3(32 * kCombineWarps), 0, s, 1, static_cast<const int*>(prm.prefix),
                     prm.plan_flags, n_tok, W, static_cast<const float*>(prm.part_o), static_cast<const float*>(prm.part_lse), prm.o_lat,
                     lse);
 }
