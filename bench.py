@@ -13,9 +13,9 @@ permutation of the pool):
   prefill_p4096  a P=4096-token prompt: query projection, cache rows, and
                causal attention over the expanded keys and values
 
-One step = the whole path for the step's new tokens: query projection with
-the cache append (mla_q_proj_append), W^UK absorption, latent attention
-(+ split combine), W^UV / W^O output.
+One step = the whole path for the step's new tokens: the latent query with
+the cache append (mla_q_latent_append: query projection, cache rows, W^UK
+absorption), latent attention (+ split combine), W^UV / W^O output.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME]
@@ -477,12 +477,13 @@ def run_ours(args):
             m.q_proj(x, W["W_dq"], W["W_uq"], W["W_qr"], bufs["q_c"], bufs["q_r"])
             m.cache_append_q8(x, W_dkr, inp["seq_idx"], inp["pos"], table, pool)
         else:
-            m.q_proj_append(x, W["W_dq"], W["W_uq"], W["W_qr"], W_dkr, inp["seq_idx"], inp["pos"], table, pool,
-                            bufs["q_c"], bufs["q_r"])
+            m.q_latent_append(x, W["W_dq"], W["W_uq"], W["W_qr"], W["W_uk"], W_dkr, inp["seq_idx"], inp["pos"],
+                              table, pool, bufs["q_lat"])
         if pairs is not None:
             eb = torch.cuda.Event(enable_timing=True, external=True)
             eb.record()
-        m.absorb_q(bufs["q_c"], bufs["q_r"], inp["pos"], W["W_uk"], bufs["q_lat"])
+        if q8:
+            m.absorb_q(bufs["q_c"], bufs["q_r"], inp["pos"], W["W_uk"], bufs["q_lat"])
         if pairs is not None:
             e0 = torch.cuda.Event(enable_timing=True, external=True)
             e0.record()
@@ -513,15 +514,16 @@ def run_ours(args):
     res_t = _measure(m, step, e2e_step, args, ws, local)
     ms, ms_plain, pairs, e2e_ms, clk, region_s = (res_t[k] for k in ("ms", "ms_plain", "pairs", "e2e_ms", "clk",
                                                                        "region_s"))
-    # per timed step: the q_proj + append part, and the decode call (plan +
+    # per timed step: the query + append part (the latent query with the
+    # cache append; the quantised cache: q_proj and its append), and the decode call (plan +
     # decode + combine), each between event nodes on the step's stream
     app_ms = sum(ea.elapsed_time(eb) for ea, eb, _, _ in pairs) / len(pairs)
     dec_ms = sum(e0.elapsed_time(e1) for _, _, e0, e1 in pairs) / len(pairs)
-    # kernels per step: query projection and append 2 (W^DQ with the cache
-    # rows; W^UQ with W^QR) -- the quantised cache: q_proj 2 and append 2
-    # (the rows, then their codes) --, absorb 1, decode 3 (plan, attention,
-    # combine), out 2 (W^UV, W^O)
-    n_launch = 10 if q8 else 8
+    # kernels per step: the latent query with the cache append 2 (W^DQ with
+    # the cache rows; W^UQ -> W^UK^T per head with W^QR) -- the quantised
+    # cache: q_proj 2, append 2 (the rows, then their codes), absorb 1 --,
+    # decode 3 (plan, attention, combine), out 2 (W^UV, W^O)
+    n_launch = 10 if q8 else 7
 
     ms, ms_plain, dec_ms, app_ms, e2e_ms = _max_over_ranks([ms, ms_plain, dec_ms, app_ms, e2e_ms], ws)
     if rank != 0:
@@ -581,7 +583,7 @@ def run_ours(args):
         "ms_per_step_without_event_nodes": round(ms_plain, 4),
         "latent_cache_gbs": round(cache_b / t / 1e9, 1),
         "decode_tokens_per_s": round(_job_rate(N, n, dec_ms), 1),
-        "q_proj_append_us": round(app_ms * 1e3, 2),
+        "query_append_us": round(app_ms * 1e3, 2),
         "roofline": roof,
         "e2e": {"value": round(_job_rate(N, n, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h_x.numel() * 2 + h_pos.numel() * 4 + h_lens.numel() * 4,

@@ -192,6 +192,11 @@ cudaError_t launch_linear_tc(const mla_handle* h, const void* X, int x_cols, con
 cudaError_t launch_linear2_tc(const mla_handle* h, const void* X, int in, const void* W1, int out1, void* Y1,
                               long long ldy1, const void* W2, int out2, void* Y2, long long ldy2, int n_tok,
                               cudaStream_t s, long long x_ld = 0, int f16_mask = 0);
+// The latent query of up to q_absorb_max_tokens() tokens straight from c^Q:
+// W^UQ_i then W^UK_i^T per head in one CTA, W^QR with RoPE in the others.
+int q_absorb_max_tokens();
+cudaError_t launch_q_absorb_tc(const mla_handle* h, const void* c_q, const void* w_uq, const void* w_qr,
+                               const void* w_uk, const int* pos, int n_tok, void* q_lat, cudaStream_t s);
 // Prefill attention over expanded keys and values (tcgen05): see mla_prefill.
 cudaError_t launch_prefill_attn_tc(const mla_handle* h, const void* rows, const void* q_c, const void* q_r, int P,
                                    const void* k_c, const void* v, void* o, float* lse, cudaStream_t s);

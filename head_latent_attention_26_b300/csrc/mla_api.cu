@@ -244,6 +244,47 @@ mla_status mla_q_proj_append(mla_handle* h, const void* x, const void* w_dq, con
   return MLA_OK;
 }
 
+// ---------------------------------------------------------------- a0 + a1 + a2 in one call
+size_t mla_q_latent_append_workspace_bytes(const mla_handle* h, int n_tok) {
+  if (!h || n_tok < 0) return 0;
+  const mla_dims& d = h->dims;
+  auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+  const size_t n = static_cast<size_t>(n_tok), e = elem_bytes(h);
+  return al(n * d.d_cq * e) + al(n * d.n_h * d.d_h * e) + al(n * d.n_h * d.d_hr * e);
+}
+
+mla_status mla_q_latent_append(mla_handle* h, const void* x, const void* w_dq, const void* w_uq, const void* w_qr,
+                               const void* w_uk, const void* w_dkr, const int* seq_idx, const int* pos, int n_tok,
+                               const int* block_table, int max_blocks, int batch, void* pool, int n_pool_blocks,
+                               void* q_lat, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!h || n_tok < 0) return MLA_ERR_INVALID_ARG;
+  if (n_tok == 0) return MLA_OK;
+  for (const void* p : {x, w_dq, w_uq, w_qr, w_uk, w_dkr, static_cast<const void*>(pool), static_cast<const void*>(q_lat)})
+    if (!p || !aligned16(p)) return MLA_ERR_INVALID_ARG;
+  if (!seq_idx || !pos || !block_table || !aligned4(seq_idx) || !aligned4(pos) || !aligned4(block_table))
+    return MLA_ERR_INVALID_ARG;
+  if (max_blocks < 1 || batch < 1 || n_pool_blocks < 1) return MLA_ERR_INVALID_ARG;
+  if (!ws || !aligned16(ws) || ws_bytes < mla_q_latent_append_workspace_bytes(h, n_tok)) return MLA_ERR_WORKSPACE;
+  const mla_dims& d = h->dims;
+  auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+  const size_t n = static_cast<size_t>(n_tok), e = elem_bytes(h);
+  uint8_t* c_q = static_cast<uint8_t*>(ws);
+  uint8_t* q_c = c_q + al(n * d.d_cq * e);
+  uint8_t* q_r = q_c + al(n * d.n_h * d.d_h * e);
+  if (h->proj_tc && h->tensor_path && n_tok <= mla::q_absorb_max_tokens()) {
+    // W^DQ with the cache rows, then W^UQ -> W^UK^T per head with W^QR + RoPE
+    MLA_TRY_CUDA(mla::launch_q_down_append_tc(h, x, w_dq, c_q, w_dkr, seq_idx, pos, n_tok, block_table, max_blocks,
+                                              batch, pool, n_pool_blocks, stream));
+    MLA_TRY_CUDA(mla::launch_q_absorb_tc(h, c_q, w_uq, w_qr, w_uk, pos, n_tok, q_lat, stream));
+    return MLA_OK;
+  }
+  // otherwise the three calls' kernels one after the other, q^C and q^R in ws
+  mla_status st = mla_q_proj_append(h, x, w_dq, w_uq, w_qr, w_dkr, seq_idx, pos, n_tok, block_table, max_blocks,
+                                    batch, pool, n_pool_blocks, q_c, q_r, c_q, al(n * d.d_cq * e), stream);
+  if (st != MLA_OK) return st;
+  return mla_absorb_q(h, q_c, q_r, pos, n_tok, w_uk, q_lat, stream);
+}
+
 // ---------------------------------------------------------------- a1, quantised cache
 size_t mla_cache_append_q8_workspace_bytes(const mla_handle* h, int n_new) {
   if (!h || n_new < 0) return 0;

@@ -58,6 +58,8 @@ _SIGS = {
     "mla_q_proj": (I, [P, P, P, P, P, I, P, P, P, SZ, P]),
     "mla_cache_append": (I, [P, P, P, P, P, I, P, I, I, P, I, P]),
     "mla_q_proj_append": (I, [P, P, P, P, P, P, P, P, I, P, I, I, P, I, P, P, P, SZ, P]),
+    "mla_q_latent_append_workspace_bytes": (SZ, [P, I]),
+    "mla_q_latent_append": (I, [P, P, P, P, P, P, P, P, P, I, P, I, I, P, I, P, P, SZ, P]),
     "mla_cache_append_q8_workspace_bytes": (SZ, [P, I]),
     "mla_cache_append_q8": (I, [P, P, P, P, P, I, P, I, I, P, I, P, SZ, P]),
     "mla_absorb_q": (I, [P, P, P, P, I, P, P, P]),
@@ -209,6 +211,19 @@ class MLA:
                                           _ptr(ws), ws.numel(), P(_stream())), "mla_q_proj_append")
         return q_c, q_r
 
+    def q_latent_append(self, x, W_dq, W_uq, W_qr, W_uk, W_dkr, seq_idx, pos, block_table, pool, q_lat=None):
+        """mla_q_latent_append: the latent query [n_tok, n_h, d_c + d_hr] of
+        the new tokens and their cache rows (q_proj + cache_append + absorb_q
+        in two launches for up to 64 tokens)."""
+        d, n = self.dims, x.shape[0]
+        q_lat = torch.empty(n, d.n_h, d.width, dtype=self.dtype, device=x.device) if q_lat is None else q_lat
+        ws = self.workspace("q_latent", self.lib.mla_q_latent_append_workspace_bytes(self.h, n))
+        _check(self.lib.mla_q_latent_append(self.h, _ptr(x), _ptr(W_dq), _ptr(W_uq), _ptr(W_qr), _ptr(W_uk),
+                                            _ptr(W_dkr), _ptr(seq_idx), _ptr(pos), n, _ptr(block_table),
+                                            block_table.shape[1], block_table.shape[0], _ptr(pool), pool.shape[0],
+                                            _ptr(q_lat), _ptr(ws), ws.numel(), P(_stream())), "mla_q_latent_append")
+        return q_lat
+
     def cache_append_q8(self, x, W_dkr, seq_idx, pos, block_table, pool_q8):
         """mla_cache_append_q8: the new tokens' rows, quantised, into a
         [n_blocks, block, 672] uint8 pool."""
@@ -313,15 +328,14 @@ class MLA:
 
     def decode_step(self, x, W: dict, W_dkr, seq_idx, pos, block_table, pool, seq_lens, cu_q,
                     num_workers: int = 0, out: dict | None = None):
-        """One whole decode step for new tokens x: project the query and
-        append the new cache rows (one call), absorb W^UK, attend over the
-        latent cache and project the output.  Returns u [n_tok, d_model]."""
+        """One whole decode step for new tokens x: the latent query and the
+        new cache rows (one call), attention over the latent cache and the
+        output projection.  Returns u [n_tok, d_model]."""
         out = {} if out is None else out
-        q_c, q_r = self.q_proj_append(x, W["W_dq"], W["W_uq"], W["W_qr"], W_dkr, seq_idx, pos, block_table, pool,
-                                      out.get("q_c"), out.get("q_r"))
-        q_lat = self.absorb_q(q_c, q_r, pos, W["W_uk"], out.get("q_lat"))
+        q_lat = self.q_latent_append(x, W["W_dq"], W["W_uq"], W["W_qr"], W["W_uk"], W_dkr, seq_idx, pos,
+                                     block_table, pool, out.get("q_lat"))
         o_lat, lse = self.decode(q_lat, pool, block_table, seq_lens, cu_q, num_workers, out.get("o_lat"),
                                  out.get("lse"))
         u = self.out(o_lat, W["W_uv"], W["W_o"], out.get("u"))
-        out.update(q_c=q_c, q_r=q_r, q_lat=q_lat, o_lat=o_lat, lse=lse, u=u)
+        out.update(q_lat=q_lat, o_lat=o_lat, lse=lse, u=u)
         return u

@@ -124,6 +124,30 @@ mla_status mla_cache_append(mla_handle* h, const void* x, const void* w_dkr, con
                             const int* pos, int n_new, const int* block_table, int max_blocks,
                             int batch, void* pool, int n_pool_blocks, cudaStream_t stream);
 
+/* ---- a0 + a1 + a2 in one call: the latent query and the cache rows --------
+ * mla_q_proj_append followed by mla_absorb_q for the same new tokens, without
+ * q^C and q^R leaving the GPU's on-chip memory when there are at most 64
+ * tokens: one launch computes c^Q = W^DQ x together with the cache rows, a
+ * second gives each head a CTA that chains q^C_i = W^UQ_i c^Q and
+ * q~_i = W^UK_i^T q^C_i ([0h-n0] "行列吸収トリック") and rotates W^QR c^Q
+ * ([qiita] "RoPE の扱い") into q_lat.  Beyond 64 tokens, or for sizes outside
+ * the tensor path, it runs the two calls' kernels.
+ *   x, w_dq, w_uq, w_qr, w_dkr, seq_idx, pos, block_table, pool: as in
+ *   mla_q_proj / mla_cache_append; w_uk as in mla_absorb_q
+ *   q_lat [n_tok, n_h, d_c + d_hr] (output)
+ *   ws: mla_q_latent_append_workspace_bytes(h, n_tok) bytes (c^Q, and q^C /
+ *       q^R when they are formed)
+ * q^C is rounded once to bf16 before the absorption, as on the separate
+ * route; the rotation of q^R is applied to its fp32 sum (the separate route
+ * rotates the stored bf16 q^R). */
+size_t mla_q_latent_append_workspace_bytes(const mla_handle* h, int n_tok);
+mla_status mla_q_latent_append(mla_handle* h, const void* x, const void* w_dq, const void* w_uq,
+                               const void* w_qr, const void* w_uk, const void* w_dkr,
+                               const int* seq_idx, const int* pos, int n_tok,
+                               const int* block_table, int max_blocks, int batch, void* pool,
+                               int n_pool_blocks, void* q_lat, void* ws, size_t ws_bytes,
+                               cudaStream_t stream);
+
 /* ---- a0 + a1 in one call ---------------------------------------------------
  * mla_q_proj and mla_cache_append for the same new tokens (x is their input
  * h, n_tok of them), with the two products that read x -- c^Q = W^DQ x and
