@@ -522,8 +522,8 @@ def run_ours(args):
     # kernels per step: the latent query with the cache append 2 (W^DQ with
     # the cache rows; W^UQ -> W^UK^T per head with W^QR) -- the quantised
     # cache: q_proj 2, append 2 (the rows, then their codes), absorb 1 --,
-    # decode 3 (plan, attention, combine), out 2 (W^UV, W^O)
-    n_launch = 10 if q8 else 7
+    # decode 3 (plan, attention, combine), out 1 (W^UV then W^O)
+    n_launch = 9 if q8 else 6
 
     ms, ms_plain, dec_ms, app_ms, e2e_ms = _max_over_ranks([ms, ms_plain, dec_ms, app_ms, e2e_ms], ws)
     if rank != 0:

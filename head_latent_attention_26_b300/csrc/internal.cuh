@@ -48,6 +48,10 @@ struct mla_handle {
   int* status;      // [4]: first device-side error code (0 = none), then where the first
                     // bounded wait gave up: site word, CTA, tile (see report_site)
   int last_site[3];  // the site words read back by the last mla_check_device_status
+  // two device counters of the one-launch output projection (CTAs past its
+  // first phase, CTAs finished), zero between calls: the words after the
+  // status word in the same allocation
+  unsigned int* out_counters;
   long long wait_limit;
   bool tensor_path;  // tcgen05 decode serves these dims
   bool proj_tc;      // tcgen05 projection kernels serve these dims
@@ -197,6 +201,11 @@ cudaError_t launch_linear2_tc(const mla_handle* h, const void* X, int in, const 
 int q_absorb_max_tokens();
 cudaError_t launch_q_absorb_tc(const mla_handle* h, const void* c_q, const void* w_uq, const void* w_qr,
                                const void* w_uk, const int* pos, int n_tok, void* q_lat, cudaStream_t s);
+// W^UV per head and W^O in one launch (up to out_fused_max_tokens() tokens);
+// cudaErrorNotSupported when it does not apply (then two launches).
+int out_fused_max_tokens();
+cudaError_t launch_out_tc(const mla_handle* h, const void* o_lat, const void* w_uv, const void* w_o, int n_tok,
+                          void* obuf, void* u, cudaStream_t s);
 // Prefill attention over expanded keys and values (tcgen05): see mla_prefill.
 cudaError_t launch_prefill_attn_tc(const mla_handle* h, const void* rows, const void* q_c, const void* q_r, int P,
                                    const void* k_c, const void* v, void* o, float* lse, cudaStream_t s);

@@ -132,15 +132,16 @@ mla_status mla_create(const mla_dims* dims, int max_pos, mla_handle** out) {
     }
   bool ok = cudaMalloc(&h->rope_cos, n * sizeof(float)) == cudaSuccess &&
             cudaMalloc(&h->rope_sin, n * sizeof(float)) == cudaSuccess &&
-            cudaMalloc(&h->status, 4 * sizeof(int)) == cudaSuccess &&
+            cudaMalloc(&h->status, 8 * sizeof(int)) == cudaSuccess &&
             cudaMemcpy(h->rope_cos, c.data(), n * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemcpy(h->rope_sin, s.data(), n * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess &&
-            cudaMemset(h->status, 0, 4 * sizeof(int)) == cudaSuccess;
+            cudaMemset(h->status, 0, 8 * sizeof(int)) == cudaSuccess;
   // The fixed scratch of mla_decode_noalloc: its device address on this
   // device, looked up now with the device current.  The lookup also loads the
   // library's device code here, so the array is reserved at creation rather
   // than at the first decode call.
   if (ok && h->tensor_path) ok = mla::decode_noalloc_scratch_address(&h->noalloc_scratch) == cudaSuccess;
+  if (ok) h->out_counters = reinterpret_cast<unsigned int*>(h->status + 4);  // words 4 and 5, zero
   if (!ok) {
     mla_destroy(h);
     return MLA_ERR_CUDA;
@@ -475,6 +476,13 @@ mla_status mla_out(mla_handle* h, const void* o_lat, const void* w_uv, const voi
   if (!ws || !aligned16(ws) || ws_bytes < mla_out_workspace_bytes(h, n_tok)) return MLA_ERR_WORKSPACE;
   const mla_dims& d = h->dims;
   const int H = d.n_h * d.d_h;
+  if (h->proj_tc && h->tensor_path && n_tok <= mla::out_fused_max_tokens()) {
+    const cudaError_t e = mla::launch_out_tc(h, o_lat, w_uv, w_o, n_tok, ws, u, stream);
+    if (e != cudaErrorNotSupported) {
+      MLA_TRY_CUDA(e);
+      return MLA_OK;
+    }
+  }
   if (h->proj_tc) {
     MLA_TRY_CUDA(mla::launch_linear_tc(h, o_lat, d.n_h * d.d_c, w_uv, d.d_c, H, d.n_h, d.d_c, ws, H, n_tok, stream));
     MLA_TRY_CUDA(mla::launch_linear_tc(h, ws, H, w_o, H, d.d_model, 1, 0, u, d.d_model, n_tok, stream));

@@ -318,7 +318,12 @@ mla_status mla_prefill(mla_handle* h, const void* rows, const void* q_c, const v
  * u = W^O [o_1; ...; o_n_h] ([qiita] "Attention 計算").
  *   o_lat [n_tok, n_h, d_c]   w_uv [n_h*d_h, d_c]   w_o [d_model, n_h*d_h]
  *   u [n_tok, d_model] (output)
- *   ws: mla_out_workspace_bytes(h, n_tok) bytes (holds the per-head o_i). */
+ *   ws: mla_out_workspace_bytes(h, n_tok) bytes (holds the per-head o_i).
+ * Up to 64 tokens at the tensor-path sizes this is one launch: every CTA
+ * first computes the o_i of one or two heads (bf16, into ws), a counter of
+ * the handle then releases the W^O phase once every CTA has done so.  Two
+ * mla_out calls of one handle must therefore not run on the GPU at the same
+ * time (other streams or threads): the handle's counters are shared. */
 size_t mla_out_workspace_bytes(const mla_handle* h, int n_tok);
 mla_status mla_out(mla_handle* h, const void* o_lat, const void* w_uv, const void* w_o,
                    int n_tok, void* u, void* ws, size_t ws_bytes, cudaStream_t stream);
