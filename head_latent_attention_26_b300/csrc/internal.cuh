@@ -58,6 +58,10 @@ struct mla_handle {
   // Device address of the decode's fixed scratch array on this handle's
   // device (looked up in mla_create with the device current), or null.
   void* noalloc_scratch;
+  // Device ranges that mla_decode calls fetch into L2 while they stream the
+  // cache (mla_set_decode_l2_prefetch); guarded by `mu`.
+  const void* l2_prefetch_ptr[2];
+  long long l2_prefetch_bytes[2];
   // Host-side launch state kept across calls so that a call does no repeated
   // driver work: encoded tensor maps and the kernels whose attributes are set.
   mutable std::mutex mu;

@@ -167,6 +167,21 @@ mla_status mla_set_wait_limit(mla_handle* h, long long polls) {
   return MLA_OK;
 }
 
+mla_status mla_set_decode_l2_prefetch(mla_handle* h, const void* const* ptrs, const size_t* bytes, int n) {
+  if (!h || n < 0 || n > 2 || (n > 0 && (!ptrs || !bytes))) return MLA_ERR_INVALID_ARG;
+  for (int r = 0; r < n; ++r)
+    if (bytes[r] && (!ptrs[r] || reinterpret_cast<uintptr_t>(ptrs[r]) % 16 || bytes[r] % 16 ||
+                     bytes[r] > (static_cast<size_t>(1) << 40)))
+      return MLA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(h->mu);
+  for (int r = 0; r < 2; ++r) {
+    const bool used = r < n && bytes[r];
+    h->l2_prefetch_ptr[r] = used ? ptrs[r] : nullptr;
+    h->l2_prefetch_bytes[r] = used ? static_cast<long long>(bytes[r]) : 0;
+  }
+  return MLA_OK;
+}
+
 // ---------------------------------------------------------------- a0
 size_t mla_q_proj_workspace_bytes(const mla_handle* h, int n_tok) {
   if (!h || n_tok < 0) return 0;

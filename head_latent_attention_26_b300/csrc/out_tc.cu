@@ -135,6 +135,8 @@ __global__ void __cluster_dims__(kOSplit, 1, 1) __launch_bounds__(kOThreads, 1)
       tma_prefetch_desc(&maps.olat);
       tma_prefetch_desc(&maps.wo);
       tma_prefetch_desc(&maps.obuf);
+      // the step's last weight reads: evict-first, also on the lines an L2
+      // prefetch brought in, so that none of them outlives the step
       const uint64_t pol_w = l2_policy_evict_first(), pol_x = l2_policy_evict_last();
       auto load_w = [&](int i, uint8_t* st, uint64_t* bar) {
         if (i < n1) {

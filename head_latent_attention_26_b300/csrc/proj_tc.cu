@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_kernel(const __grid_constant
     if (lane == 0) {
       tma_prefetch_desc(wmap);
       tma_prefetch_desc(&maps.x);
-      const uint64_t pol_w = l2_policy_evict_first(), pol_x = l2_policy_evict_last();
+      const uint64_t pol_w = l2_policy_evict_normal(), pol_x = l2_policy_evict_last();
       const int x_off = group * p.x_group_cols;
       // The weights do not depend on earlier kernels: the first STAGES weight
       // tiles go out before the wait for the previous kernel, their token

@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kQThreads, 2)  // two CTAs per SM: 128 registe
       tma_prefetch_desc(head_cta ? &maps.wuq : &maps.wqr);
       tma_prefetch_desc(&maps.cq);
       if (head_cta) tma_prefetch_desc(&maps.wuk);
-      const uint64_t pol_w = l2_policy_evict_first(), pol_x = l2_policy_evict_last();
+      const uint64_t pol_w = l2_policy_evict_normal(), pol_x = l2_policy_evict_last();
       // load i: phase-1 weight tile (i < nk) or W^UK_i^T tile (m, kb) of phase 2
       auto stage_bytes = [&](int i) { return i < nk ? kQStage : kQA; };
       auto load_w = [&](int i, uint8_t* st, uint64_t* bar) {

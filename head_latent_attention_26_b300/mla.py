@@ -20,6 +20,24 @@ from .synth import Dims
 
 HEADER = os.path.join(ROOT, "include", "mla.h")
 
+#: Bytes of the output projection's weights a decode step has the attention
+#: fetch into L2 (a 126 MB L2 keeps about this much of a normal-priority
+#: prefetch alive beside the evict-first cache stream).
+OUT_WEIGHT_PREFETCH_BYTES = 96 << 20
+
+
+def output_weight_prefetch(W_uv: torch.Tensor, W_o: torch.Tensor, budget_bytes: int) -> tuple:
+    """Ranges for MLA.set_decode_l2_prefetch ahead of the output projection:
+    W^UV whole (its first phase reads it) and then the leading whole 128-row
+    tiles of W^O, at most budget_bytes in all; () for a budget of 0."""
+    uv = W_uv.numel() * W_uv.element_size()
+    if budget_bytes <= 0:
+        return ()
+    if budget_bytes <= uv:
+        return (W_uv.reshape(-1)[:budget_bytes // 16 * 16 // W_uv.element_size()],)
+    rows = min(W_o.shape[0], (budget_bytes - uv) // (W_o.shape[1] * W_o.element_size()) // 128 * 128)
+    return (W_uv, W_o[:rows]) if rows > 0 else (W_uv,)
+
 MLA_OK = 0
 STATUS = {
     0: "MLA_OK",
@@ -54,6 +72,7 @@ _SIGS = {
     "mla_num_sms": (I, [P]),
     "mla_uses_tensor_path": (I, [P]),
     "mla_set_wait_limit": (I, [P, LL]),
+    "mla_set_decode_l2_prefetch": (I, [P, ctypes.POINTER(P), ctypes.POINTER(SZ), I]),
     "mla_q_proj_workspace_bytes": (SZ, [P, I]),
     "mla_q_proj": (I, [P, P, P, P, P, I, P, P, P, SZ, P]),
     "mla_cache_append": (I, [P, P, P, P, P, I, P, I, I, P, I, P]),
@@ -161,6 +180,19 @@ class MLA:
 
     def set_wait_limit(self, polls: int):
         _check(self.lib.mla_set_wait_limit(self.h, polls), "mla_set_wait_limit")
+
+    def set_decode_l2_prefetch(self, *ranges):
+        """Device ranges (contiguous tensors or tensor views; at most two)
+        that later decode calls fetch into L2 while they stream the cache,
+        for the kernel that follows them (the output projection's weights);
+        no argument clears.  The tensors are kept alive while they are set."""
+        ptrs, sizes = (P * max(2, len(ranges)))(), (SZ * max(2, len(ranges)))()
+        for i, t in enumerate(ranges):
+            if not t.is_contiguous():
+                raise ValueError("an L2 prefetch range must be contiguous")
+            ptrs[i], sizes[i] = t.data_ptr(), t.numel() * t.element_size()
+        _check(self.lib.mla_set_decode_l2_prefetch(self.h, ptrs, sizes, len(ranges)), "mla_set_decode_l2_prefetch")
+        self._l2_prefetch = tuple(ranges)
 
     def check(self):
         """Synchronise and raise if any kernel recorded a device-side error."""
@@ -327,15 +359,25 @@ class MLA:
         return u
 
     def decode_step(self, x, W: dict, W_dkr, seq_idx, pos, block_table, pool, seq_lens, cu_q,
-                    num_workers: int = 0, out: dict | None = None):
+                    num_workers: int = 0, out: dict | None = None,
+                    l2_prefetch_bytes: int = OUT_WEIGHT_PREFETCH_BYTES):
         """One whole decode step for new tokens x: the latent query and the
         new cache rows (one call), attention over the latent cache and the
-        output projection.  Returns u [n_tok, d_model]."""
+        output projection.  While the attention streams the cache it fetches
+        up to l2_prefetch_bytes of W^UV and W^O into L2 for the output
+        projection (tensor path; 0 = none).  Returns u [n_tok, d_model]."""
         out = {} if out is None else out
         q_lat = self.q_latent_append(x, W["W_dq"], W["W_uq"], W["W_qr"], W["W_uk"], W_dkr, seq_idx, pos,
                                      block_table, pool, out.get("q_lat"))
-        o_lat, lse = self.decode(q_lat, pool, block_table, seq_lens, cu_q, num_workers, out.get("o_lat"),
-                                 out.get("lse"))
+        ranges = output_weight_prefetch(W["W_uv"], W["W_o"], l2_prefetch_bytes) if self.tensor_path else ()
+        if ranges:
+            self.set_decode_l2_prefetch(*ranges)
+        try:
+            o_lat, lse = self.decode(q_lat, pool, block_table, seq_lens, cu_q, num_workers, out.get("o_lat"),
+                                     out.get("lse"))
+        finally:
+            if ranges:
+                self.set_decode_l2_prefetch()
         u = self.out(o_lat, W["W_uv"], W["W_o"], out.get("u"))
         out.update(q_lat=q_lat, o_lat=o_lat, lse=lse, u=u)
         return u

@@ -244,6 +244,30 @@ mla_status mla_decode(mla_handle* h, const void* q_lat, const void* pool, int n_
                       const int* cu_q, int batch, int n_tok, int num_workers, void* ws,
                       size_t ws_bytes, void* o_lat, float* lse, cudaStream_t stream);
 
+/* ---- L2 prefetch during the attention --------------------------------------
+ * Not on the pages: a scheduling aid for the step of [qiita] "Attention 計算",
+ * whose output projection u = W^O [o_1; ...; o_nh] (with o_i = W^UV_i o~_i,
+ * [kasblo] "V側は、小さな表現の加重和を先に求める") reads its weights right
+ * after the attention.  The attention leaves HBM bandwidth unused, so later
+ * mla_decode and mla_decode_q8 calls on this handle fetch up to two device
+ * ranges into L2 while they stream the cache, spread evenly over the call:
+ * the ranges end to end are cut into one piece per 64-row tile of the call
+ * and per SM of the pair that loads it.  The cache is read at evict-first
+ * priority and the prefetch lands at normal priority, so what fits in L2
+ * beside the other normal-priority data is still there when the next kernel
+ * on the stream reads it.  The query-side projection kernels read their
+ * weights at normal priority too: a step's query weights replace the lines
+ * the previous step prefetched, so each step fetches its ranges from HBM
+ * again.
+ * Only addresses and sizes are kept: the ranges must stay valid while such
+ * calls run, and nothing reads them for results (a stale range costs
+ * bandwidth only).
+ *   ptrs[n], bytes[n]  n <= 2; each pointer 16-byte aligned, each size a
+ *                      multiple of 16 (0 = unused); n = 0 clears.
+ * Returns MLA_ERR_INVALID_ARG otherwise.  mla_decode_noalloc does not
+ * prefetch.  Thread-safe against concurrent calls on the handle. */
+mla_status mla_set_decode_l2_prefetch(mla_handle* h, const void* const* ptrs, const size_t* bytes, int n);
+
 /* ---- a3 + a4 over the quantised latent cache -------------------------------
  * The attention of mla_decode with the cache rows of mla_cache_append_q8
  * ([0h-n0] "量子化との組み合わせ"): row j stands for [code_j * scale_(j/32) ;
