@@ -50,15 +50,16 @@ from head_latent_attention_26_b300 import synth  # noqa: E402
 METRIC = "MLA decode tokens/s and latent-cache GB/s (% of HBM/tensor roofline), 1×B300"
 
 # DRAM bytes (read + write) of one decode_tc_kernel launch on the B=64, T=4096
-# workload, from an ncu capture of the kernel sources with these hashes; the
-# figure is reported only while the sources still hash to them.
-PROFILED_DECODE = {"sources": {"decode_tc.cu": "661b9209bf3c159d", "ptx.cuh": "1fd1dc657a7fe061"},
-                   "workload": (64, 4096), "traffic_bytes": 314375168}
+# workload with the given L2 prefetch, from an ncu capture of the kernel
+# sources with these hashes; the figure is reported only while the sources
+# still hash to them.
+PROFILED_DECODE = {"sources": {"decode_tc.cu": "4594af35cf9b4dfa", "ptx.cuh": "c59e8751e182f4db"},
+                   "workload": (64, 4096), "l2_prefetch_bytes": 100663296, "traffic_bytes": 415685632}
 
 
-def _profiled_traffic(B: int, T: int):
+def _profiled_traffic(B: int, T: int, pf_bytes: int):
     import hashlib
-    if (B, T) != PROFILED_DECODE["workload"]:
+    if (B, T, pf_bytes) != (*PROFILED_DECODE["workload"], PROFILED_DECODE["l2_prefetch_bytes"]):
         return None
     csrc = os.path.join(ROOT, "head_latent_attention_26_b300", "csrc")
     for name, digest in PROFILED_DECODE["sources"].items():
@@ -446,13 +447,18 @@ L2_PREFETCH_MB_DEFAULT = 96.0
 
 def l2_prefetch_setup(m, W, mb: float):
     """Has the decode fetch W^UV and the leading rows of W^O (whole 128-row
-    tiles, up to `mb` MB in all) into L2; returns a description."""
+    tiles, up to `mb` MB in all) into L2; returns a description and the
+    bytes."""
     from head_latent_attention_26_b300 import mla
     ranges = mla.output_weight_prefetch(W["W_uv"], W["W_o"], int(mb * 2**20))
     m.set_decode_l2_prefetch(*ranges)
+    return _prefetch_desc(W, ranges), sum(t.numel() * t.element_size() for t in ranges)
+
+
+def _prefetch_desc(W, ranges):
     if not ranges:
         return "none"
-    desc = f"W^UV ({W['W_uv'].numel() * 2 / 1e6:.1f} MB)"
+    desc = f"W^UV ({ranges[0].numel() * 2 / 1e6:.1f} MB)"
     if len(ranges) == 2:
         desc += f" and W^O rows 0..{ranges[1].shape[0] - 1} ({ranges[1].numel() * 2 / 1e6:.1f} MB)"
     return desc + " fetched into L2 during the decode for the output projection of the same step"
@@ -484,7 +490,7 @@ def run_ours(args):
         "u": torch.empty(N, d.d_model, dtype=torch.bfloat16, device="cuda"),
     }
     ws_dec = m.workspace("decode", m.decode_workspace_bytes(N, args.num_workers))
-    pf_desc = l2_prefetch_setup(m, W, args.l2_prefetch_mb)
+    pf_desc, pf_bytes = l2_prefetch_setup(m, W, args.l2_prefetch_mb)
     x_dev = torch.empty_like(inp["x"])
     x_dev.copy_(inp["x"])
 
@@ -571,11 +577,13 @@ def run_ours(args):
     else:
         roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4)}
     traffic = args.traffic if args.traffic is not None else (
-        None if q8 else _profiled_traffic(B, lens[0] if len(set(lens)) == 1 else -1))
+        None if q8 else _profiled_traffic(B, lens[0] if len(set(lens)) == 1 else -1, pf_bytes))
     roof.update(kernel="decode_tc_kernel<quantised> (+plan, combine)" if q8 else "decode_tc_kernel (+plan, combine)",
                 peak_source=f"{src} (MEASURED_PEAKS.json), "
                 f"tensor peak {tc_kind} (timed region {region_s * 1e3:.1f} ms)",
                 traffic=traffic,
+                # the decode launch also reads these bytes for the next kernel (in `traffic`, not in `achieved`)
+                l2_prefetch_bytes=pf_bytes,
                 other={"hbm": {"achieved_gbs": round(gbs, 1), "peak": hbm, "frac": round(gbs / hbm, 4)},
                        "tensor": {"achieved_tflops": round(tflops, 1), "peak_sustained": tf_sus,
                                   "peak_burst": tf_burst, "frac_sustained": round(tflops / tf_sus, 4),

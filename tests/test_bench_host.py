@@ -31,13 +31,16 @@ def test_algorithmic_work_scales_linearly():
 
 
 def test_profiled_traffic_guard():
-    # the capture's traffic is reported only for its workload and sources
-    assert bench._profiled_traffic(64, 2048) is None
-    t = bench._profiled_traffic(64, 4096)
+    # the capture's traffic is reported only for its workload, L2 prefetch and sources
+    pf = bench.PROFILED_DECODE["l2_prefetch_bytes"]
+    assert bench._profiled_traffic(64, 2048, pf) is None
+    assert bench._profiled_traffic(64, 4096, pf + 16) is None
+    t = bench._profiled_traffic(64, 4096, pf)
     assert t is None or t == bench.PROFILED_DECODE["traffic_bytes"]
-    # within a few percent of the algorithmic bytes: the cache is read once
+    # within a few percent of the algorithmic bytes plus the prefetched ones:
+    # the cache is read once
     _, total, _ = bench.algorithmic(64, 4096)
-    assert abs(bench.PROFILED_DECODE["traffic_bytes"] / total - 1) < 0.03
+    assert abs(bench.PROFILED_DECODE["traffic_bytes"] / (total + pf) - 1) < 0.03
 
 
 @pytest.mark.parametrize("units,ws,ms,expect", [(64, 1, 0.2, 320000.0), (64, 4, 0.25, 1024000.0)])
