@@ -440,9 +440,6 @@ def _measure(m, step, e2e_step, args, ws: int, local: int) -> dict:
     return dict(ms=ms, ms_plain=ms_plain, pairs=pairs, e2e_ms=e2e_ms, clk=clk, region_s=region_s)
 
 
-# The decode streams the cache at about half the HBM rate; the rest fetches
-# the output projection's weights into L2 for the kernel that follows it.
-L2_PREFETCH_MB_DEFAULT = 96.0
 
 
 def l2_prefetch_setup(m, W, mb: float):
@@ -490,7 +487,11 @@ def run_ours(args):
         "u": torch.empty(N, d.d_model, dtype=torch.bfloat16, device="cuda"),
     }
     ws_dec = m.workspace("decode", m.decode_workspace_bytes(N, args.num_workers))
-    pf_desc, pf_bytes = l2_prefetch_setup(m, W, args.l2_prefetch_mb)
+    # the decode streams the cache at about half the HBM rate; the rest
+    # fetches the output projection's weights into L2 for the kernel that
+    # follows it (by default where that pays: steps of up to 64 tokens)
+    pf_mb = args.l2_prefetch_mb if args.l2_prefetch_mb is not None else mla.default_prefetch_bytes(N) / 2**20
+    pf_desc, pf_bytes = l2_prefetch_setup(m, W, pf_mb)
     x_dev = torch.empty_like(inp["x"])
     x_dev.copy_(inp["x"])
 
@@ -946,9 +947,9 @@ def main():
     ap.add_argument("--batch", type=int, default=None, help="override B of a uniform workload")
     ap.add_argument("--seq-len", type=int, default=None, help="override T of a uniform workload")
     ap.add_argument("--num-workers", type=int, default=0)
-    ap.add_argument("--l2-prefetch-mb", type=float, default=L2_PREFETCH_MB_DEFAULT,
+    ap.add_argument("--l2-prefetch-mb", type=float, default=None,
                     help="W^UV and leading W^O rows the decode fetches into L2 for the output projection "
-                         "(0 = none)")
+                         "(0 = none; default: 96 MiB for steps of up to 64 tokens, else none)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,

@@ -24,6 +24,16 @@ HEADER = os.path.join(ROOT, "include", "mla.h")
 #: fetch into L2 (a 126 MB L2 keeps about this much of a normal-priority
 #: prefetch alive beside the evict-first cache stream).
 OUT_WEIGHT_PREFETCH_BYTES = 96 << 20
+#: Steps of more tokens than this run the output projection as two launches
+#: and their decode re-reads more of its own data through L2 (queries, split
+#: partials); there the prefetch cost the decode more than it saved (a ragged
+#: batch of 194 tokens: decode +12 µs, output projection -1.9 µs).
+OUT_WEIGHT_PREFETCH_MAX_TOKENS = 64
+
+
+def default_prefetch_bytes(n_tok: int) -> int:
+    """The L2 prefetch budget decode_step uses for a step of n_tok tokens."""
+    return OUT_WEIGHT_PREFETCH_BYTES if n_tok <= OUT_WEIGHT_PREFETCH_MAX_TOKENS else 0
 
 
 def output_weight_prefetch(W_uv: torch.Tensor, W_o: torch.Tensor, budget_bytes: int) -> tuple:
@@ -360,13 +370,16 @@ class MLA:
 
     def decode_step(self, x, W: dict, W_dkr, seq_idx, pos, block_table, pool, seq_lens, cu_q,
                     num_workers: int = 0, out: dict | None = None,
-                    l2_prefetch_bytes: int = OUT_WEIGHT_PREFETCH_BYTES):
+                    l2_prefetch_bytes: int | None = None):
         """One whole decode step for new tokens x: the latent query and the
         new cache rows (one call), attention over the latent cache and the
         output projection.  While the attention streams the cache it fetches
         up to l2_prefetch_bytes of W^UV and W^O into L2 for the output
-        projection (tensor path; 0 = none).  Returns u [n_tok, d_model]."""
+        projection (tensor path; None = default_prefetch_bytes(n_tok), 0 =
+        none).  Returns u [n_tok, d_model]."""
         out = {} if out is None else out
+        if l2_prefetch_bytes is None:
+            l2_prefetch_bytes = default_prefetch_bytes(x.shape[0])
         q_lat = self.q_latent_append(x, W["W_dq"], W["W_uq"], W["W_qr"], W["W_uk"], W_dkr, seq_idx, pos,
                                      block_table, pool, out.get("q_lat"))
         ranges = output_weight_prefetch(W["W_uv"], W["W_o"], l2_prefetch_bytes) if self.tensor_path else ()

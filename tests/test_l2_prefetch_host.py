@@ -38,3 +38,9 @@ def test_output_weight_prefetch_ranges(weights, budget):
 
 def test_prefetch_binding_is_declared():
     assert "mla_set_decode_l2_prefetch" in mla.header_symbols()
+
+
+def test_default_prefetch_only_for_one_launch_output_steps():
+    # steps whose output projection is the one-launch kernel (up to 64 tokens)
+    assert mla.default_prefetch_bytes(1) == mla.default_prefetch_bytes(64) == mla.OUT_WEIGHT_PREFETCH_BYTES
+    assert mla.default_prefetch_bytes(65) == mla.default_prefetch_bytes(194) == 0
