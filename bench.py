@@ -591,7 +591,10 @@ def run_ours(args):
                                   "frac_burst": round(tflops / tf_burst, 4)}},
                 algorithmic_bytes=dec_bytes, algorithmic_flops=flops, decode_us=round(dec_ms * 1e3, 2))
     n = ws
-    value = _job_rate(N, n, ms)
+    # the headline: the K steps replayed with nothing between the kernels but
+    # the stream order (the event nodes that time each call in the other
+    # replay break the kernels' programmatic overlap)
+    value = _job_rate(N, n, ms_plain)
     res = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -599,7 +602,7 @@ def run_ours(args):
         "n_gpus": n,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms, 4),
+        "ms_per_step": round(ms_plain, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -612,9 +615,10 @@ def run_ours(args):
                    "l2": f"no flush: every step streams {(298_024_960 + cache_b) / 1e6:.0f} MB of weights and "
                          "cache, more than the 126 MB L2",
                    "l2_prefetch": pf_desc,
-                   "timing": "K steps captured as CUDA graphs of the C-ABI calls and replayed; events around "
-                             "each step's decode call inside the graphs"},
-        "ms_per_step_without_event_nodes": round(ms_plain, 4),
+                   "timing": "K steps captured as CUDA graphs of the C-ABI calls and replayed, timed by events "
+                             "around the replays; the per-call times come from a second capture of the same "
+                             "steps with event nodes around each call"},
+        "ms_per_step_with_event_nodes": round(ms, 4),
         "latent_cache_gbs": round(cache_b / t / 1e9, 1),
         "decode_tokens_per_s": round(_job_rate(N, n, dec_ms), 1),
         "query_append_us": round(app_ms * 1e3, 2),
@@ -724,12 +728,12 @@ def run_prefill(args):
     n = ws
     res = {
         "metric": METRIC,
-        "value": round(_job_rate(P, n, ms), 1),
+        "value": round(_job_rate(P, n, ms_plain), 1),
         "unit": "tokens/s",
         "n_gpus": n,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms, 4),
+        "ms_per_step": round(ms_plain, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -741,9 +745,10 @@ def run_prefill(args):
                    "parallelism": f"replicas x{n}" if n > 1 else "single GPU",
                    "l2": "no flush: the step writes and reads the expanded K^C and V "
                          f"({2 * P * d.n_h * d.d_h * 2 / 1e6:.0f} MB), more than the 126 MB L2",
-                   "timing": "K steps captured as CUDA graphs of the C-ABI calls and replayed; events around "
-                             "each step's prefill call inside the graphs"},
-        "ms_per_step_without_event_nodes": round(ms_plain, 4),
+                   "timing": "K steps captured as CUDA graphs of the C-ABI calls and replayed, timed by events "
+                             "around the replays; the prefill call's time comes from a second capture of the "
+                             "same steps with event nodes around it"},
+        "ms_per_step_with_event_nodes": round(ms, 4),
         "prefill_tokens_per_s": round(_job_rate(P, n, pre_ms), 1),
         "roofline": roof,
         "e2e": {"value": round(_job_rate(P, n, e2e_ms), 1), "unit": "tokens/s",
