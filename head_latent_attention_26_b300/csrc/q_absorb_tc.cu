@@ -241,10 +241,14 @@ __global__ void __launch_bounds__(kQThreads, 2)  // two CTAs per SM: 128 registe
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bs->qc_ready);
-        if ((ok = qa_wait(&bs->done, 0, p, bs, 5))) {
+        if ((ok = qa_wait_warp(&bs->done, 0, p, bs, 5))) {
           tc_fence_after();
-          // q~_i: latent column 128 m + r of every token
-          __nv_bfloat16* base = p.q_lat + static_cast<size_t>(head) * kQWidth + r;
+          // q~_i: this warp holds latent columns 128 m + 32 w + lane (m = 0..3)
+          // of every token.  They go through the warp's 16 KB of the (now
+          // idle) stages, [token][m][32 columns], and leave as 16-byte pieces
+          // (the four 64-byte runs of each token's row), 32 stores a lane
+          // instead of 256 two-byte ones.
+          uint8_t* stg = smem + w * (kQn * kQLatBlocks * 64);
 #pragma unroll 1
           for (int m = 0; m < kQLatBlocks; ++m) {
             uint32_t q[kQn];
@@ -253,28 +257,52 @@ __global__ void __launch_bounds__(kQThreads, 2)  // two CTAs per SM: 128 registe
             tmem_ld_wait();
 #pragma unroll
             for (int n = 0; n < kQn; ++n)
-              if (n < p.n_tok)
-                base[static_cast<size_t>(n) * p.n_h * kQWidth + m * kQm] = __float2bfloat16_rn(__uint_as_float(q[n]));
+              *reinterpret_cast<__nv_bfloat16*>(stg + n * (kQLatBlocks * 64) + m * 64 + lane * 2) =
+                  __float2bfloat16_rn(__uint_as_float(q[n]));
+          }
+          __syncwarp();
+          for (int i = lane; i < p.n_tok * kQLatBlocks * 4; i += 32) {
+            const int n = i / (kQLatBlocks * 4), m = (i / 4) % kQLatBlocks, piece = i % 4;
+            *reinterpret_cast<uint4*>(p.q_lat + (static_cast<size_t>(n) * p.n_h + head) * kQWidth + m * kQm + 32 * w +
+                                      8 * piece) =
+                *reinterpret_cast<const uint4*>(stg + n * (kQLatBlocks * 64) + m * 64 + piece * 16);
           }
         }
       } else {
         // W^QR row 128 rtile + r = positional column k2 of head hq; the pair
         // (2k, 2k + 1) sits in adjacent lanes and turns by pos * theta_k
+        // Eight tokens at a time: their positions, then their cos / sin,
+        // every load of a group in flight before the group's products (one
+        // token after another, each load waited on, took a round trip each).
         const int o = rtile * kQm + r, hq = o / kQDhr, k2 = o % kQDhr, k = k2 >> 1;
+        constexpr int kG = 8;
 #pragma unroll
-        for (int n = 0; n < kQn; ++n) {
-          if (n >= p.n_tok) break;
-          const float x = __uint_as_float(v[n]);
-          const float y = __shfl_xor_sync(0xffffffffu, x, 1);
-          const int tp = __ldg(p.pos + n);
-          if (tp < 0 || tp >= p.max_pos) {
-            if (k2 == 0) report(p.status, MLA_ERR_DEVICE_BOUNDS);
-            continue;
+        for (int n0 = 0; n0 < kQn; n0 += kG) {
+          if (n0 >= p.n_tok) break;
+          int tp[kG];
+#pragma unroll
+          for (int i = 0; i < kG; ++i) tp[i] = n0 + i < p.n_tok ? __ldg(p.pos + n0 + i) : 0;
+          float cs[kG], sn[kG];
+#pragma unroll
+          for (int i = 0; i < kG; ++i) {
+            const bool in = tp[i] >= 0 && tp[i] < p.max_pos;
+            const size_t t = static_cast<size_t>(in ? tp[i] : 0) * (kQDhr / 2) + k;
+            cs[i] = __ldg(p.rope_cos + t);
+            sn[i] = __ldg(p.rope_sin + t);
           }
-          const size_t t = static_cast<size_t>(tp) * (kQDhr / 2) + k;
-          const float cs = __ldg(p.rope_cos + t), sn = __ldg(p.rope_sin + t);
-          const float out = (k2 & 1) ? y * sn + x * cs : x * cs - y * sn;
-          p.q_lat[(static_cast<size_t>(n) * p.n_h + hq) * kQWidth + kQDc + k2] = __float2bfloat16_rn(out);
+#pragma unroll
+          for (int i = 0; i < kG; ++i) {
+            const int n = n0 + i;
+            if (n >= p.n_tok) break;
+            const float x = __uint_as_float(v[n]);
+            const float y = __shfl_xor_sync(0xffffffffu, x, 1);
+            if (tp[i] < 0 || tp[i] >= p.max_pos) {
+              if (k2 == 0) report(p.status, MLA_ERR_DEVICE_BOUNDS);
+              continue;
+            }
+            const float out = (k2 & 1) ? y * sn[i] + x * cs[i] : x * cs[i] - y * sn[i];
+            p.q_lat[(static_cast<size_t>(n) * p.n_h + hq) * kQWidth + kQDc + k2] = __float2bfloat16_rn(out);
+          }
         }
       }
     }
