@@ -36,7 +36,8 @@ constexpr uint32_t kOB = kOn * kOk * 2;   // 8 KB token tile
 constexpr uint32_t kOStage = kOA + kOB;
 constexpr int kOStages = 8;
 constexpr uint32_t kOOffBars = kOStages * kOStage;
-constexpr uint32_t kOSmem = kOOffBars + 256 + 1024;
+constexpr uint32_t kOOffStg = kOOffBars + 256;         // phase 1: 4 KB per epilogue warp, [token][32 columns]
+constexpr uint32_t kOSmem = kOOffStg + 4 * kOn * 64 + 1024;
 constexpr int kOThreads = 256;
 constexpr int kOMaxHeadsPerCta = 2;
 constexpr int kOSplit = 3;                // cluster size along the k range of W^O
@@ -249,18 +250,28 @@ __global__ void __cluster_dims__(kOSplit, 1, 1) __launch_bounds__(kOThreads, 1)
     if (lane == 0) pdl_wait();  // the scratch and u may still be read by the previous kernel
     __syncwarp();
     bool ok = true;
+    // o_i column 32 w + lane of every token, through this warp's 4 KB of
+    // staging ([token][32 columns]), then as 16-byte pieces (the 64-byte run
+    // of each token's row this warp owns): 8 stores a lane, not 64 two-byte ones
+    uint8_t* stg = smem + kOOffStg + w * (kOn * 64);
     for (int hs = 0; hs < n_heads && ok; ++hs) {
-      if (!(ok = ot_wait(&bs->p1_done[hs], 0, p, bs, 4))) break;
+      if (!(ok = ot_wait_warp(&bs->p1_done[hs], 0, p, bs, 4))) break;
       tc_fence_after();
       uint32_t v[kOn];
       tmem_ld32(tmem + lanes + hs * kOn, v);
       tmem_ld32(tmem + lanes + hs * kOn + 32, v + 32);
       tmem_ld_wait();
       const int hd = cta + hs * p.ctas;
-      __nv_bfloat16* dst = p.obuf + static_cast<size_t>(hd) * kOm + r;  // o_i column r of every token
 #pragma unroll
       for (int n = 0; n < kOn; ++n)
-        if (n < p.n_tok) dst[static_cast<size_t>(n) * p.n_h * kOm] = __float2bfloat16_rn(__uint_as_float(v[n]));
+        *reinterpret_cast<__nv_bfloat16*>(stg + n * 64 + lane * 2) = __float2bfloat16_rn(__uint_as_float(v[n]));
+      __syncwarp();
+      for (int i = lane; i < p.n_tok * 4; i += 32) {
+        const int n = i >> 2, piece = i & 3;
+        *reinterpret_cast<uint4*>(p.obuf + static_cast<size_t>(n) * p.n_h * kOm + static_cast<size_t>(hd) * kOm +
+                                  32 * w + 8 * piece) = *reinterpret_cast<const uint4*>(stg + n * 64 + piece * 16);
+      }
+      __syncwarp();  // the staging is reused by the next head
     }
     // this CTA's o columns are stored: count it (all 128 epilogue threads
     // fence their stores, meet, and one of them adds)
